@@ -1,0 +1,702 @@
+// Split-KV GQA decode kernel for sm_103a (TMA + tcgen05 + TMEM).
+//
+// One persistent CTA per SM walks the work items of plan.cuh.  Per 128-position
+// KV block of one (batch, KV head) pair it computes, with the operands swapped
+// so that KV positions fill the MMA M dimension and the query-head group fills
+// N ("Building a Faster GQA Decode Kernel for Blackwell SM100", section
+// "Starting with the simple pipeline"):
+//
+//     S^T[128 x N] = K_blk[128 x d] Q^T[d x N]          (TMEM, fp32)
+//     P^T          = exp2(S^T * scale*log2e - m)       (online softmax)
+//     O^T[d x N]  += V_blk^T[d x 128] P^T[128 x N]     (TMEM, fp32)
+//
+// N = nq*G padded to 16 or 32; column n is query token n / G, head n % G of
+// the group (the PackGQA row order of "Flash Attention 4 - warp-role
+// choreography and the edges", section "Edge 2 - GQA").
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q per item, then K/V tiles into an mbarrier ring
+//               in the order K0 K1 V0 K2 V1 ... (the page's split-local order),
+//               so the score MMA of block i+1 can run while block i's softmax
+//               is in flight;
+//   warp 1      MMA issuer (one thread): QK(i+1) into the other of two S slots
+//               before PV(i) (the S/P ping-pong of "Optimization diaries: S/P
+//               ping-pong for FlashAttention-4 decode"); owns the TMEM
+//               allocation;
+//   warps 2..5  softmax / correction / epilogue warpgroup: thread r owns TMEM
+//               lane r = KV position r of S^T and row r of O^T.  It releases
+//               the S slot as soon as the scores are in registers, masks,
+//               votes on whether any column's max moved by more than the
+//               rescale threshold (8 in log2 units, "Flash Attention 4 -
+//               warp-role choreography and the edges", section "The
+//               correction"), and only then reduces the column max and
+//               rescales O in TMEM.  P goes to shared memory in one handoff
+//               as the K-major B operand of the PV MMA; the denominator is
+//               summed per lane in registers and reduced once per item.
+//
+// head_dim 64 uses M = 128 for the PV MMA by stacking the two 64-position
+// halves of the block along M: A = [V_lo^T ; V_hi^T] (128 x 64), B =
+// [P_lo ; P_hi] (2N x 64).  Lanes 0..63 x columns [0, N) then hold the first
+// half's contribution and lanes 64..127 x columns [N, 2N) the second's; the
+// cross quadrants are discarded and the epilogue adds the two halves.
+//
+// Every wait is bounded.  A wait that times out sets the device error word,
+// raises a CTA-wide abort flag and the roles leave their loops in step (the
+// softmax warps decide uniformly, at their exchange barriers), wait for their
+// own copies and MMAs in flight and free TMEM before returning.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "plan.cuh"
+#include "sm103_ptx.cuh"
+
+namespace gqa {
+
+enum : unsigned { kErrTimeout = 1u, kErrBadSeqlen = 2u };
+
+// Device error word of this library: bits of kErrTimeout / kErrBadSeqlen,
+// read and cleared by the host through gqa_decode_get_error().
+__device__ unsigned int g_gqa_error_bits = 0;
+
+constexpr int kThreads = 192;
+constexpr int kMaxSmemB = 1024;      // sequences whose lengths are staged in shared memory
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kSCol0 = 0, kSCol1 = 32, kOCol = 64;
+
+struct DecodeParams {
+  CUtensorMap tm_q;  // q [B, nq, Hq, d] bf16, box {64, G, nq, 1}
+  CUtensorMap tm_k;  // k_cache [B, S_max, Hkv, d] bf16, box {64, 1, 128, 1}
+  CUtensorMap tm_v;  // v_cache, same
+  const int32_t* seqlens;
+  void* out;          // [B, nq, Hq, d] bf16 or fp32
+  float* lse;         // [B, nq, Hq] or null
+  float* o_part;      // [slots, B*nq*Hq, d]
+  float* lse_part;    // [slots, B*nq*Hq]
+  int32_t* n_pieces;  // [B*Hkv] (PLAN_BALANCED)
+  PlanParams plan;
+  int nq, Hq, G, head_dim;
+  int out_fp32;
+  int causal;
+  float scale_log2;   // softmax scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+template <int HEAD_DIM, int NPAD>
+struct DecodeCfg {
+  static constexpr int kChunks = HEAD_DIM / 64;            // 128-byte swizzle atoms along d
+  static constexpr int kSlotBytes = kBlockN * HEAD_DIM * 2;  // one K or V block
+  static constexpr int kQBytes = kChunks * NPAD * 128;       // one Q buffer
+  static constexpr int kPBytes = 2 * NPAD * 128;             // one P buffer (two 64-position atoms)
+  static constexpr int kOWidth = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // TMEM columns of O
+  // fixed part of shared memory after the ring
+  static constexpr int kXchgBytes = 2 * (4 * 4 + 4 * NPAD * 4);
+  static constexpr int kMiscBytes = 512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64;
+  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes;
+  static constexpr int kSmemBudget = 227 * 1024 - 1024;  // minus alignment slack
+  static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kSlotBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kRingBytes = kStages * kSlotBytes;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kFixedBytes;
+  static_assert(kStages >= 4, "ring too shallow");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory over budget");
+  static_assert(kOWidth <= 64 && NPAD <= 32, "TMEM column plan");
+};
+
+namespace detail {
+
+// Reduces NP per-lane values across the 32 lanes of a warp, column by column.
+// Afterwards lane l holds the reduction of column transpose_col<NP>(l).
+template <int NP, bool IS_MAX>
+__device__ __forceinline__ float transpose_reduce(const float (&v)[NP], int lane) {
+  float a[NP];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) a[i] = v[i];
+  int off = 16;
+#pragma unroll
+  for (int w = NP / 2; w >= 1; w /= 2) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float mine = upper ? a[w + j] : a[j];
+      const float other = upper ? a[j] : a[w + j];
+      const float recv = __shfl_xor_sync(0xffffffffu, other, off);
+      a[j] = IS_MAX ? fmaxf(mine, recv) : mine + recv;
+    }
+    off >>= 1;
+  }
+#pragma unroll
+  for (; off >= 1; off >>= 1) {
+    const float recv = __shfl_xor_sync(0xffffffffu, a[0], off);
+    a[0] = IS_MAX ? fmaxf(a[0], recv) : a[0] + recv;
+  }
+  return a[0];
+}
+
+template <int NP>
+__device__ __forceinline__ int transpose_col(int lane) {
+  int col = 0, off = 16;
+#pragma unroll
+  for (int w = NP / 2; w >= 1; w /= 2) {
+    if (lane & off) col += w;
+    off >>= 1;
+  }
+  return col;
+}
+
+__device__ __forceinline__ void set_error(unsigned bits, volatile int* abort_flag) {
+  atomicOr(&g_gqa_error_bits, bits);
+  if (abort_flag != nullptr) *abort_flag = 1;
+}
+
+}  // namespace detail
+
+template <int HEAD_DIM, int NPAD>
+__global__ void __launch_bounds__(kThreads, 1)
+gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
+  using Cfg = DecodeCfg<HEAD_DIM, NPAD>;
+  constexpr int NS = Cfg::kStages;
+  constexpr int KCH = Cfg::kChunks;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* qbuf = ring + Cfg::kRingBytes;                // 2 x kQBytes
+  uint8_t* pbuf = qbuf + 2 * Cfg::kQBytes;               // 2 x kPBytes
+  uint8_t* misc = pbuf + 2 * Cfg::kPBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(misc);     // 64 barrier words max
+  uint32_t* xflags = reinterpret_cast<uint32_t*>(misc + 512);         // [2][4]
+  float* xvals = reinterpret_cast<float*>(misc + 512 + 32);            // [2][4][NPAD]
+  int32_t* s_len = reinterpret_cast<int32_t*>(misc + 512 + Cfg::kXchgBytes);  // [kMaxSmemB]
+  int32_t* s_pre = s_len + kMaxSmemB;                                   // [kMaxSmemB + 1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_pre + kMaxSmemB + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* scan_tmp = reinterpret_cast<int32_t*>(tmem_slot + 2);      // [6] warp totals
+
+  // barrier indices
+  const uint32_t bar_base = ptx::smem_u32(bar);
+  auto BAR = [&](int i) -> uint32_t { return bar_base + 8u * static_cast<uint32_t>(i); };
+  const int RING_FULL = 0, RING_EMPTY = NS, Q_FULL = 2 * NS, Q_EMPTY = 2 * NS + 2,
+            S_FULL = 2 * NS + 4, S_EMPTY = 2 * NS + 6, P_FULL = 2 * NS + 8, P_EMPTY = 2 * NS + 10,
+            DRAIN = 2 * NS + 12;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = p.plan.batch;
+  const bool lens_in_smem = B <= kMaxSmemB;
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      ptx::mbar_init(BAR(RING_FULL + i), 1);
+      ptx::mbar_init(BAR(RING_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(BAR(Q_FULL + i), 1);
+      ptx::mbar_init(BAR(Q_EMPTY + i), 1);
+      ptx::mbar_init(BAR(S_FULL + i), 1);
+      ptx::mbar_init(BAR(S_EMPTY + i), 4);
+      ptx::mbar_init(BAR(P_FULL + i), 4);
+      ptx::mbar_init(BAR(P_EMPTY + i), 1);
+    }
+    ptx::mbar_init(BAR(DRAIN), 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&p.tm_q);
+    ptx::prefetch_tensormap(&p.tm_k);
+    ptx::prefetch_tensormap(&p.tm_v);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  // Padding rows of Q (beyond nq*G) and both P buffers start at zero; TMA
+  // never writes them.
+  {
+    const int nv = p.nq * p.G;
+    for (int i = threadIdx.x; i < 2 * KCH * NPAD; i += kThreads) {
+      const int row = i % NPAD;
+      if (row < nv) continue;
+      uint4* dst = reinterpret_cast<uint4*>(qbuf + (i / NPAD) * NPAD * 128 + row * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+    uint4* pz = reinterpret_cast<uint4*>(pbuf);
+    for (int i = threadIdx.x; i < 2 * Cfg::kPBytes / 16; i += kThreads) pz[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  // Inputs may be produced by the previous kernel in the stream.
+  ptx::griddep_wait();
+
+  if (lens_in_smem) {
+    // clamped lengths, and (balanced plan) exclusive prefix sums of block counts
+    constexpr int kCh = (kMaxSmemB + kThreads - 1) / kThreads;
+    int nb[kCh];
+    int local = 0;
+    const int i0 = threadIdx.x * kCh;
+#pragma unroll
+    for (int j = 0; j < kCh; ++j) {
+      const int i = i0 + j;
+      nb[j] = 0;
+      if (i < B) {
+        const int raw = p.seqlens[i];
+        const int L = clamp_len(raw, p.plan.max_seqlen);
+        if (raw != L) detail::set_error(kErrBadSeqlen, nullptr);
+        s_len[i] = L;
+        nb[j] = num_blocks(L);
+        local += nb[j];
+      }
+    }
+    if (p.plan.mode == PLAN_BALANCED) {
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) scan_tmp[warp] = incl;
+      __syncthreads();
+      int base = 0;
+      for (int w = 0; w < warp; ++w) base += scan_tmp[w];
+      int run = base + incl - local;
+#pragma unroll
+      for (int j = 0; j < kCh; ++j) {
+        const int i = i0 + j;
+        if (i < B) s_pre[i] = run;
+        run += nb[j];
+      }
+      if (i0 < B && i0 + kCh >= B) s_pre[B] = run;
+      if (B == 0 && threadIdx.x == 0) s_pre[0] = 0;
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int32_t* lens_raw = lens_in_smem ? s_len : p.seqlens;
+
+  // =============================================================== producer
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t policy = ptx::l2_policy_evict_first();
+      uint32_t t = 0;   // tiles issued into the ring
+      int kq = 0;       // non-empty items
+      bool have_prev = false, ok = true;
+      int pb = 0, ph = 0, pblk = 0;
+      // last tile issued per ring stage, for the drain on abort
+      auto load_tile = [&](const CUtensorMap* map, int b, int h, int blk) -> bool {
+        const uint32_t stage = t % NS, phase = (t / NS) & 1u;
+        if (!ptx::mbar_wait_bounded(BAR(RING_EMPTY + stage), phase ^ 1u, abort_flag, p.timeout_ns))
+          return false;
+        ptx::mbar_arrive_expect_tx(BAR(RING_FULL + stage), Cfg::kSlotBytes);
+        uint8_t* dst = ring + stage * Cfg::kSlotBytes;
+#pragma unroll
+        for (int kc = 0; kc < KCH; ++kc)
+          ptx::tma_load_4d_hint(ptx::smem_u32(dst + kc * 16384), map, BAR(RING_FULL + stage), kc * 64, h,
+                                blk * kBlockN, b, policy);
+        ++t;
+        return true;
+      };
+      WorkIter iter;
+      iter.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+      WorkItem it;
+      while (ok && iter.next(it)) {
+        if (it.blk_begin >= it.blk_end) continue;
+        const int qb = kq & 1;
+        if (!ptx::mbar_wait_bounded(BAR(Q_EMPTY + qb), ((kq >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(BAR(Q_FULL + qb), KCH * p.nq * p.G * 128);
+#pragma unroll
+        for (int kc = 0; kc < KCH; ++kc)
+          ptx::tma_load_4d(ptx::smem_u32(qbuf + qb * Cfg::kQBytes + kc * NPAD * 128), &p.tm_q,
+                           BAR(Q_FULL + qb), kc * 64, it.h * p.G, 0, it.b);
+        ++kq;
+        for (int blk = it.blk_begin; blk < it.blk_end && ok; ++blk) {
+          ok = load_tile(&p.tm_k, it.b, it.h, blk);
+          if (ok && have_prev) ok = load_tile(&p.tm_v, pb, ph, pblk);
+          pb = it.b; ph = it.h; pblk = blk; have_prev = true;
+        }
+      }
+      if (ok && have_prev) ok = load_tile(&p.tm_v, pb, ph, pblk);
+      if (!ok) {
+        detail::set_error(kErrTimeout, abort_flag);
+        // let the copies already issued land before the CTA exits
+        const uint32_t first = t > static_cast<uint32_t>(NS) ? t - NS : 0u;
+        for (uint32_t u = first; u < t; ++u)
+          ptx::mbar_wait_bounded(BAR(RING_FULL + u % NS), (u / NS) & 1u, nullptr, p.timeout_ns);
+        for (int k = (kq > 2 ? kq - 2 : 0); k < kq; ++k)
+          ptx::mbar_wait_bounded(BAR(Q_FULL + (k & 1)), (k >> 1) & 1, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  }
+  // ============================================================ MMA issuer
+  else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, NPAD, 0, 0);
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, Cfg::kOWidth, 1, 0);
+      uint32_t t = 0;  // tiles consumed
+      uint32_t g = 0;  // blocks
+      int kq = 0;
+      bool ok = true, have_prev = false;
+      uint32_t prev_g = 0;
+      bool prev_first = false;
+      auto issue_pv = [&](uint32_t gg, bool first_of_item) -> bool {
+        const uint32_t sl = gg & 1u;
+        if (!ptx::mbar_wait_bounded(BAR(P_FULL + sl), (gg >> 1) & 1u, abort_flag, p.timeout_ns)) return false;
+        const uint32_t vt = t++;
+        const uint32_t stage = vt % NS;
+        if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (vt / NS) & 1u, abort_flag, p.timeout_ns))
+          return false;
+        ptx::tc_fence_after();
+        const uint32_t v_addr = ptx::smem_u32(ring + stage * Cfg::kSlotBytes);
+        const uint32_t p_addr = ptx::smem_u32(pbuf + sl * Cfg::kPBytes);
+        if constexpr (HEAD_DIM == 128) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t a = ptx::smem_desc_sw128(v_addr + k * 2048, 16384, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(p_addr + (k >> 2) * (NPAD * 128) + (k & 3) * 32, 16, 1024);
+            ptx::mma_bf16_ss(tmem_base + kOCol, a, bd, idesc_pv, (k > 0 || !first_of_item) ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = ptx::smem_desc_sw128(v_addr + k * 2048, 8192, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(p_addr + k * 32, 16, 1024);
+            ptx::mma_bf16_ss(tmem_base + kOCol, a, bd, idesc_pv, (k > 0 || !first_of_item) ? 1u : 0u);
+          }
+        }
+        ptx::mma_commit(BAR(P_EMPTY + sl));
+        ptx::mma_commit(BAR(RING_EMPTY + stage));
+        return true;
+      };
+      WorkIter iter;
+      iter.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+      WorkItem it;
+      while (ok && iter.next(it)) {
+        if (it.blk_begin >= it.blk_end) continue;
+        const int qb = kq & 1;
+        if (!ptx::mbar_wait_bounded(BAR(Q_FULL + qb), (kq >> 1) & 1, abort_flag, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t q_addr = ptx::smem_u32(qbuf + qb * Cfg::kQBytes);
+        for (int blk = it.blk_begin; blk < it.blk_end; ++blk) {
+          const uint32_t sl = g & 1u;
+          ok = ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns);
+          const uint32_t kt = t++;
+          const uint32_t stage = kt % NS;
+          ok = ok && ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (kt / NS) & 1u, abort_flag, p.timeout_ns);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t k_addr = ptx::smem_u32(ring + stage * Cfg::kSlotBytes);
+          const uint32_t s_col = sl ? kSCol1 : kSCol0;
+#pragma unroll
+          for (int k = 0; k < HEAD_DIM / 16; ++k) {
+            const uint64_t a = ptx::smem_desc_sw128(k_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+            const uint64_t bq = ptx::smem_desc_sw128(q_addr + (k >> 2) * (NPAD * 128) + (k & 3) * 32, 16, 1024);
+            ptx::mma_bf16_ss(tmem_base + s_col, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(BAR(S_FULL + sl));
+          ptx::mma_commit(BAR(RING_EMPTY + stage));
+          if (blk == it.blk_end - 1) ptx::mma_commit(BAR(Q_EMPTY + qb));
+          if (have_prev) {
+            ok = issue_pv(prev_g, prev_first);
+            if (!ok) break;
+          }
+          prev_g = g;
+          prev_first = (blk == it.blk_begin);
+          have_prev = true;
+          ++g;
+        }
+        ++kq;
+      }
+      if (ok && have_prev) ok = issue_pv(prev_g, prev_first);
+      if (!ok) detail::set_error(kErrTimeout, abort_flag);
+      // every MMA issued has completed before TMEM is released
+      ptx::mma_commit(BAR(DRAIN));
+      ptx::mbar_wait_bounded(BAR(DRAIN), 0, nullptr, p.timeout_ns);
+    }
+    __syncwarp();
+  }
+  // ===================================================== softmax warpgroup
+  else {
+    const int tq = warp & 3;          // TMEM lane quarter of this warp
+    const int r = tq * 32 + lane;     // TMEM lane = KV row of S^T = row of O^T
+    const uint32_t lane_addr = static_cast<uint32_t>(tq * 32) << 16;
+    const int nv = p.nq * p.G;        // valid columns
+    const int rows_total = p.plan.batch * p.nq * p.Hq;
+    bool local_abort = false;
+    uint32_t xc = 0;                  // exchange counter
+
+    // Exchange: every warp posts flags (lane 0) and, optionally, per-column
+    // values (lane l posts column transpose_col(l)); after the barrier all
+    // four warps see the same data.  Returns the OR of the flags.
+    auto exchange = [&](uint32_t flags, bool with_vals, float val) -> uint32_t {
+      const uint32_t buf = xc & 1u;
+      ++xc;
+      if (lane == 0) xflags[buf * 4 + tq] = flags;
+      if (with_vals) {
+        const int col = detail::transpose_col<NPAD>(lane);
+        if (NPAD == 32 || (lane & 1) == 0) xvals[(buf * 4 + tq) * NPAD + col] = val;
+      }
+      ptx::named_barrier_sync(1, 128);
+      return xflags[buf * 4 + 0] | xflags[buf * 4 + 1] | xflags[buf * 4 + 2] | xflags[buf * 4 + 3];
+    };
+    auto xval = [&](int w, int col) -> float { return xvals[(((xc - 1) & 1u) * 4 + w) * NPAD + col]; };
+
+    // total blocks of this CTA (to locate the last V tile in the ring)
+    uint32_t g_total = 0;
+    {
+      WorkIter it0;
+      it0.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+      WorkItem w0;
+      while (it0.next(w0)) g_total += static_cast<uint32_t>(w0.blk_end - w0.blk_begin);
+    }
+
+    WorkIter iter;
+    iter.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+    WorkItem it;
+    uint32_t g = 0;
+    bool aborted = false;
+    while (!aborted && iter.next(it)) {
+      const int b = it.b, h = it.h;
+      const long long pair = static_cast<long long>(b) * p.plan.kv_heads + h;
+      if (it.first_piece && p.n_pieces != nullptr && threadIdx.x == 64) p.n_pieces[pair] = it.n_pieces;
+      if (it.blk_begin >= it.blk_end) {
+        // empty item: final output O = 0, lse = -inf; partial lse = -inf
+        for (int n = 0; n < nv; ++n) {
+          const int t = n / p.G, hq = h * p.G + n % p.G;
+          const long long row = (static_cast<long long>(b) * p.nq + t) * p.Hq + hq;
+          if (it.slot < 0) {
+            if (r < HEAD_DIM) {
+              if (p.out_fp32) static_cast<float*>(p.out)[row * HEAD_DIM + r] = 0.f;
+              else static_cast<__nv_bfloat16*>(p.out)[row * HEAD_DIM + r] = __float2bfloat16_rn(0.f);
+            }
+            if (r == 0 && p.lse != nullptr) p.lse[row] = -INFINITY;
+          } else if (r == 0) {
+            p.lse_part[static_cast<long long>(it.slot) * rows_total + row] = -INFINITY;
+          }
+        }
+        continue;
+      }
+      const int L = it.L;
+      float m[NPAD], l[NPAD];
+#pragma unroll
+      for (int n = 0; n < NPAD; ++n) { m[n] = -INFINITY; l[n] = 0.f; }
+
+      for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
+        const bool first = (blk == it.blk_begin);
+        const uint32_t sl = g & 1u;
+        // ---- scores
+        float x[NPAD];
+        if (!local_abort)
+          local_abort = !ptx::mbar_wait_bounded(BAR(S_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns);
+        local_abort = __any_sync(0xffffffffu, local_abort);
+        ptx::tc_fence_after();
+        if (!local_abort) {
+          const uint32_t s_col = sl ? kSCol1 : kSCol0;
+#pragma unroll
+          for (int c = 0; c < NPAD; c += 16) {
+            float v16[16];
+            ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + s_col + c, v16);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[c + i] = v16[i];
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n) x[n] = -INFINITY;
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !local_abort) ptx::mbar_arrive(BAR(S_EMPTY + sl));  // S slot free for QK(g+2)
+
+        // ---- mask: position pos is visible to column n when pos < L and,
+        // with the causal mask, n / G >= pos - (L - nq)  (bottom-right)
+        const int pos = blk * kBlockN + r;
+        int n_min = 0;
+        if (p.causal) {
+          const int ahead = pos - (L - p.nq);
+          n_min = ahead > 0 ? ahead * p.G : 0;
+        }
+        const bool row_valid = pos < L;
+        bool need = false;
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) {
+          const bool vis = row_valid && n >= n_min && n < nv;
+          x[n] = vis ? x[n] * p.scale_log2 : -INFINITY;
+          need |= x[n] > m[n] + kRescaleThreshold;
+        }
+        const uint32_t fl = exchange((__any_sync(0xffffffffu, need) ? 1u : 0u) | (local_abort ? 2u : 0u), false, 0.f);
+        if (fl & 2u) { aborted = true; break; }
+
+        // ---- correction (only when some column's max moved past the threshold)
+        if (fl & 1u) {
+          const float wmax = detail::transpose_reduce<NPAD, true>(x, lane);
+          if (!first && !local_abort) {
+            // O may be rescaled only after PV(g-1) has landed
+            local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u,
+                                                  abort_flag, p.timeout_ns);
+          }
+          local_abort = __any_sync(0xffffffffu, local_abort);
+          const uint32_t f2 = exchange(local_abort ? 2u : 0u, true, wmax);
+          if (f2 & 2u) { aborted = true; break; }
+          float alpha[NPAD];
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n) {
+            const float bm = fmaxf(fmaxf(xval(0, n), xval(1, n)), fmaxf(xval(2, n), xval(3, n)));
+            const float mn = fmaxf(m[n], bm);
+            const float ms = mn == -INFINITY ? 0.f : mn;
+            alpha[n] = ptx::ex2_approx(m[n] - ms);
+            m[n] = mn;
+            l[n] *= alpha[n];
+          }
+          if (!first) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < Cfg::kOWidth; c += 16) {
+              float o16[16];
+              ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + kOCol + c, o16);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o16[i] *= alpha[(c + i) % NPAD];
+              ptx::tmem_st_32x32b_x16(tmem_base + lane_addr + kOCol + c, o16);
+            }
+            ptx::tmem_wait_st();
+          }
+        }
+
+        // ---- probabilities; the denominator is accumulated per lane
+        float pr[NPAD];
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) {
+          const float ms = m[n] == -INFINITY ? 0.f : m[n];
+          pr[n] = ptx::ex2_approx(x[n] - ms);
+          l[n] += pr[n];
+        }
+        // P buffer sl is free once PV(g-2) has completed
+        if (!local_abort)
+          local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns);
+        local_abort = __any_sync(0xffffffffu, local_abort);
+        if (!local_abort) {
+          // P^T as the K-major B operand: row n, position r, 128-byte swizzle
+          uint8_t* pb = pbuf + sl * Cfg::kPBytes + (r >> 6) * (NPAD * 128);
+          const int chunk = (r & 63) >> 3, within = (r & 7) * 2;
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n) {
+            const int sw = chunk ^ (n & 7);
+            *reinterpret_cast<__nv_bfloat16*>(pb + n * 128 + sw * 16 + within) = __float2bfloat16_rn(pr[n]);
+          }
+          // Tail block: V rows past the sequence end hold whatever the cache
+          // holds there; zero them so that 0 * garbage cannot poison O.
+          const int tail_rows = L - blk * kBlockN;
+          const int cap_rows = p.plan.max_seqlen - blk * kBlockN;
+          if (tail_rows < kBlockN && cap_rows > tail_rows) {
+            const uint32_t vt = (g + 1 < g_total) ? 2u * g + 2u : 2u * g + 1u;
+            const uint32_t stage = vt % NS;
+            local_abort = !ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (vt / NS) & 1u, abort_flag, p.timeout_ns);
+            local_abort = __any_sync(0xffffffffu, local_abort);
+            if (!local_abort && r >= tail_rows && r < cap_rows) {
+#pragma unroll
+              for (int kc = 0; kc < KCH; ++kc) {
+                uint4* row = reinterpret_cast<uint4*>(ring + stage * Cfg::kSlotBytes + kc * 16384 + r * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+              }
+            }
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !local_abort) ptx::mbar_arrive(BAR(P_FULL + sl));
+      }
+      if (aborted) break;
+
+      // ---------------------------------------------------------- epilogue
+      const uint32_t gl = g - 1;
+      if (!local_abort)
+        local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag, p.timeout_ns);
+      local_abort = __any_sync(0xffffffffu, local_abort);
+      const float lsum = detail::transpose_reduce<NPAD, false>(l, lane);
+      const uint32_t f3 = exchange(local_abort ? 2u : 0u, true, lsum);
+      if (f3 & 2u) { aborted = true; break; }
+      float lt[NPAD];
+#pragma unroll
+      for (int n = 0; n < NPAD; ++n) lt[n] = (xval(0, n) + xval(1, n)) + (xval(2, n) + xval(3, n));
+
+      ptx::tc_fence_after();
+      float o[Cfg::kOWidth];
+#pragma unroll
+      for (int c = 0; c < Cfg::kOWidth; c += 16) {
+        float o16[16];
+        ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + kOCol + c, o16);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[c + i] = o16[i];
+      }
+      ptx::tc_fence_before();
+      int d_row = r;
+      bool writer = true;
+      if constexpr (HEAD_DIM == 64) {
+        // lanes 64..127 hold the second half-block's contribution in columns [N, 2N)
+        float* xo = reinterpret_cast<float*>(pbuf);  // both P buffers are idle here
+        if (r >= 64) {
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n) xo[(r - 64) * NPAD + n] = o[NPAD + n];
+        }
+        ptx::named_barrier_sync(1, 128);
+        if (r < 64) {
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n) o[n] += xo[r * NPAD + n];
+        }
+        ptx::named_barrier_sync(1, 128);  // xo is read before P is rewritten
+        writer = r < 64;
+      }
+      if (writer) {
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) {
+          if (n >= nv) break;
+          const int t = n / p.G, hq = h * p.G + n % p.G;
+          const long long row = (static_cast<long long>(b) * p.nq + t) * p.Hq + hq;
+          const float inv = lt[n] > 0.f ? 1.0f / lt[n] : 0.f;
+          const float val = o[n] * inv;
+          if (it.slot < 0) {
+            if (p.out_fp32) static_cast<float*>(p.out)[row * HEAD_DIM + d_row] = val;
+            else static_cast<__nv_bfloat16*>(p.out)[row * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
+          } else {
+            p.o_part[(static_cast<long long>(it.slot) * rows_total + row) * HEAD_DIM + d_row] = val;
+          }
+          if (d_row == n) {
+            const float lse = lt[n] > 0.f ? 0.69314718055994531f * (m[n] + __log2f(lt[n])) : -INFINITY;
+            if (it.slot < 0) {
+              if (p.lse != nullptr) p.lse[row] = lse;
+            } else {
+              p.lse_part[static_cast<long long>(it.slot) * rows_total + row] = lse;
+            }
+          }
+        }
+      }
+    }
+    if (aborted || local_abort) detail::set_error(kErrTimeout, abort_flag);
+    // results of this CTA are written: dependents may launch
+    ptx::griddep_launch_dependents();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace gqa

@@ -1,0 +1,483 @@
+// Host side of the C ABI declared in include/gqa_decode.h: argument checks,
+// split planning, TMA tensor-map encoding and the decode / combine launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gqa_decode.h"
+#include "combine_kernel.cuh"
+#include "decode_kernel.cuh"
+#include "plan.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kWsAlign = 256;
+
+struct DeviceState {
+  int sm_count = 0;
+  unsigned attr_done = 0;  // one bit per kernel instantiation
+};
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
+unsigned long long wait_timeout_ns() {
+  const char* v = std::getenv("GQA_WAIT_TIMEOUT_MS");
+  if (v != nullptr) {
+    const long long ms = std::atoll(v);
+    if (ms > 0) return static_cast<unsigned long long>(ms) * 1000000ull;
+  }
+  return 1000000000ull;  // one second: decode launches take microseconds
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+gqa_status_t current_device(int* dev, DeviceState** st) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[*dev];
+  if (s.sm_count == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess || n <= 0)
+      return GQA_ERR_CUDA;
+    s.sm_count = n;
+  }
+  *st = &s;
+  return GQA_OK;
+}
+
+// Sets the dynamic shared memory limit of a kernel once per device.
+gqa_status_t ensure_smem_attr(DeviceState* st, unsigned bit, const void* fn, int bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->attr_done & (1u << bit)) return GQA_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  st->attr_done |= 1u << bit;
+  return GQA_OK;
+}
+
+gqa_status_t check_desc(const gqa_desc_t* d) {
+  if (d == nullptr) return GQA_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->q_tokens < 1 || d->q_heads < 1 || d->kv_heads < 1 || d->max_seqlen < 1)
+    return GQA_ERR_INVALID_ARG;
+  if (d->q_heads % d->kv_heads != 0) return GQA_ERR_INVALID_ARG;
+  if (d->out_dtype != GQA_DTYPE_BF16 && d->out_dtype != GQA_DTYPE_FP32) return GQA_ERR_INVALID_ARG;
+  if (!(d->scale >= 0.f) || std::isinf(d->scale)) return GQA_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return GQA_ERR_UNSUPPORTED;
+  const long long g = d->q_heads / d->kv_heads;
+  if (static_cast<long long>(d->q_tokens) * g > GQA_MAX_QROWS) return GQA_ERR_UNSUPPORTED;
+  if (d->q_heads > 65535 || d->max_seqlen > (1 << 30)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+struct HostPlan {
+  PlanParams pp;
+  int num_slots;      // partial slots per row (0: the decode writes final outputs only)
+  bool combine;       // a combine launch follows
+  bool use_n_pieces;  // combine reads per-pair piece counts (balanced plan)
+};
+
+// Automatic split count for the fixed-splits plan, from a load model that
+// assumes every sequence is max_seqlen long: the busiest CTA's blocks plus
+// the partial traffic spread over the GPU.
+int auto_splits(long long pairs, int nblk, int rows_per_pair, int head_dim, int sm) {
+  double best = 1e300;
+  int best_s = 1;
+  for (int S = 1; S <= GQA_MAX_SPLITS && S <= (nblk > 0 ? nblk : 1); S *= 2) {
+    const long long items = pairs * S;
+    const long long waves = (items + sm - 1) / sm;
+    const int per_item = (nblk + S - 1) / S;
+    const double kv = static_cast<double>(waves) * per_item * kBlockN * head_dim * 4.0;
+    const double part = S > 1 ? static_cast<double>(items) * rows_per_pair * head_dim * 8.0 / sm : 0.0;
+    const double cost = kv + part;
+    if (cost < best * 0.98) { best = cost; best_s = S; }
+  }
+  return best_s;
+}
+
+HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_partial) {
+  HostPlan hp;
+  std::memset(&hp, 0, sizeof hp);
+  PlanParams& pp = hp.pp;
+  pp.batch = d->batch;
+  pp.kv_heads = d->kv_heads;
+  pp.max_seqlen = d->max_seqlen;
+  const int nblk_cap = num_blocks(d->max_seqlen);
+  const long long pairs = static_cast<long long>(d->batch) * d->kv_heads;
+  const int rows_per_pair = d->q_tokens * (d->q_heads / d->kv_heads);
+  if (num_splits == 0 && d->batch <= kMaxSmemB) {
+    pp.mode = PLAN_BALANCED;
+    long long units_cap = pairs * nblk_cap;
+    if (units_cap < 1) units_cap = 1;
+    pp.num_ctas = static_cast<int>(units_cap < sm ? units_cap : sm);
+    pp.num_splits = 0;
+    pp.min_blocks = 1;
+    const int slots = pp.num_ctas < nblk_cap ? pp.num_ctas : nblk_cap;
+    hp.num_slots = slots >= 2 ? slots : 0;
+    hp.combine = hp.num_slots >= 2;
+    hp.use_n_pieces = true;
+    return hp;
+  }
+  pp.mode = PLAN_SPLITS;
+  pp.num_splits = num_splits > 0 ? num_splits : auto_splits(pairs, nblk_cap, rows_per_pair, d->head_dim, sm);
+  pp.min_blocks = 1;
+  pp.force_partial = force_partial ? 1 : 0;
+  long long items = pairs * pp.num_splits;
+  if (items < 1) items = 1;
+  pp.num_ctas = static_cast<int>(items < sm ? items : sm);
+  hp.num_slots = (pp.num_splits == 1 && !force_partial) ? 0 : pp.num_splits;
+  hp.combine = pp.num_splits > 1 && !force_partial;
+  hp.use_n_pieces = false;
+  return hp;
+}
+
+struct WsLayout {
+  size_t o_off, lse_off, np_off, total;
+};
+
+WsLayout ws_layout(const gqa_desc_t* d, const HostPlan& hp) {
+  WsLayout w{0, 0, 0, 0};
+  if (!hp.combine) return w;
+  const size_t rows = static_cast<size_t>(d->batch) * d->q_tokens * d->q_heads;
+  const size_t slots = static_cast<size_t>(hp.num_slots);
+  w.o_off = 0;
+  w.lse_off = round_up(slots * rows * d->head_dim * sizeof(float), kWsAlign);
+  w.np_off = w.lse_off + round_up(slots * rows * sizeof(float), kWsAlign);
+  w.total = w.np_off + round_up(static_cast<size_t>(d->batch) * d->kv_heads * sizeof(int32_t), kWsAlign);
+  return w;
+}
+
+gqa_status_t encode_maps(const gqa_desc_t* d, const void* q, const void* k, const void* v, DecodeParams* p) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return GQA_ERR_CUDA;
+  const cuuint64_t D = static_cast<cuuint64_t>(d->head_dim);
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const int G = d->q_heads / d->kv_heads;
+  {
+    const cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(d->q_heads), static_cast<cuuint64_t>(d->q_tokens),
+                                static_cast<cuuint64_t>(d->batch)};
+    const cuuint64_t strides[3] = {D * 2, D * 2 * d->q_heads, D * 2 * d->q_heads * d->q_tokens};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(d->q_tokens), 1};
+    if (enc(&p->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return GQA_ERR_INVALID_ARG;
+  }
+  const cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(d->kv_heads), static_cast<cuuint64_t>(d->max_seqlen),
+                              static_cast<cuuint64_t>(d->batch)};
+  const cuuint64_t strides[3] = {D * 2, D * 2 * d->kv_heads, D * 2 * d->kv_heads * d->max_seqlen};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBlockN), 1};
+  CUtensorMap* maps[2] = {&p->tm_k, &p->tm_v};
+  const void* ptrs[2] = {k, v};
+  for (int i = 0; i < 2; ++i) {
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptrs[i]), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return GQA_ERR_INVALID_ARG;
+  }
+  return GQA_OK;
+}
+
+cudaLaunchAttribute pdl_attr(bool on) {
+  cudaLaunchAttribute a;
+  std::memset(&a, 0, sizeof a);
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = on ? 1 : 0;
+  return a;
+}
+
+template <int HD, int NP>
+gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodeParams& p, cudaStream_t s) {
+  using Cfg = DecodeCfg<HD, NP>;
+  const void* fn = reinterpret_cast<const void*>(&gqa_decode_kernel<HD, NP>);
+  gqa_status_t rc = ensure_smem_attr(st, attr_bit, fn, Cfg::kSmemBytes);
+  if (rc != GQA_OK) return rc;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.plan.num_ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HD, NP>, p) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+gqa_status_t launch_decode(DeviceState* st, const DecodeParams& p, cudaStream_t s) {
+  const int nv = p.nq * p.G;
+  if (p.head_dim == 64) {
+    return nv <= 16 ? launch_decode_t<64, 16>(st, 0, p, s) : launch_decode_t<64, 32>(st, 1, p, s);
+  }
+  return nv <= 16 ? launch_decode_t<128, 16>(st, 2, p, s) : launch_decode_t<128, 32>(st, 3, p, s);
+}
+
+gqa_status_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t s) {
+  if (c.rows == 0) return GQA_OK;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  const long long rows_per_cta = kCombineThreads / 32;
+  const long long grid = (c.rows + rows_per_cta - 1) / rows_per_cta;
+  if (grid > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, gqa_combine_kernel<64>, c)
+                                 : cudaLaunchKernelEx(&cfg, gqa_combine_kernel<128>, c);
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t check_inputs(const void* q, const void* k, const void* v, const int32_t* seqlens) {
+  if (q == nullptr || k == nullptr || v == nullptr || seqlens == nullptr) return GQA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(seqlens, 4)) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+// Common front half of gqa_decode_attn / gqa_decode_splitkv.
+gqa_status_t prepare_decode(const gqa_desc_t* d, const void* q, const void* k, const void* v,
+                            const int32_t* seqlens, const HostPlan& hp, DecodeParams* p) {
+  std::memset(p, 0, sizeof *p);
+  gqa_status_t rc = encode_maps(d, q, k, v, p);
+  if (rc != GQA_OK) return rc;
+  p->seqlens = seqlens;
+  p->plan = hp.pp;
+  p->nq = d->q_tokens;
+  p->Hq = d->q_heads;
+  p->G = d->q_heads / d->kv_heads;
+  p->head_dim = d->head_dim;
+  p->out_fp32 = d->out_dtype == GQA_DTYPE_FP32;
+  p->causal = d->causal != 0;
+  const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
+  p->scale_log2 = scale * 1.4426950408889634f;
+  p->timeout_ns = wait_timeout_ns();
+  return GQA_OK;
+}
+
+__global__ void selftest_wait_kernel(unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on this barrier: the wait must give up on its own.
+  const bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&bar), 0, nullptr, timeout_ns);
+  if (!ok && threadIdx.x == 0) atomicOr(&g_gqa_error_bits, kErrTimeout);
+}
+
+}  // namespace
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+size_t gqa_decode_workspace_size(const gqa_desc_t* desc, int num_splits) {
+  if (check_desc(desc) != GQA_OK || num_splits < 0 || num_splits > GQA_MAX_SPLITS) return 0;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  if (current_device(&dev, &st) != GQA_OK) return 0;
+  const HostPlan hp = make_plan(desc, num_splits, st->sm_count, false);
+  return ws_layout(desc, hp).total;
+}
+
+gqa_status_t gqa_decode_attn(const gqa_desc_t* desc, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* seqlens, void* out, float* lse, int num_splits, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  gqa_status_t rc = check_desc(desc);
+  if (rc != GQA_OK) return rc;
+  if (num_splits < 0 || num_splits > GQA_MAX_SPLITS) return GQA_ERR_INVALID_ARG;
+  if (desc->batch == 0) return GQA_OK;  // nothing to compute; pointers may be null
+  if ((rc = check_inputs(q, k_cache, v_cache, seqlens)) != GQA_OK) return rc;
+  if (out == nullptr || !aligned(out, 16) || (lse != nullptr && !aligned(lse, 4))) return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  if ((rc = current_device(&dev, &st)) != GQA_OK) return rc;
+  const HostPlan hp = make_plan(desc, num_splits, st->sm_count, false);
+  const WsLayout wl = ws_layout(desc, hp);
+  if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total || !aligned(workspace, kWsAlign)))
+    return GQA_ERR_WORKSPACE;
+  DecodeParams p;
+  if ((rc = prepare_decode(desc, q, k_cache, v_cache, seqlens, hp, &p)) != GQA_OK) return rc;
+  p.out = out;
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (hp.combine) {
+    p.o_part = reinterpret_cast<float*>(ws + wl.o_off);
+    p.lse_part = reinterpret_cast<float*>(ws + wl.lse_off);
+    if (hp.use_n_pieces) p.n_pieces = reinterpret_cast<int32_t*>(ws + wl.np_off);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_decode(st, p, s)) != GQA_OK) return rc;
+  if (!hp.combine) return GQA_OK;
+  CombineParams c;
+  std::memset(&c, 0, sizeof c);
+  c.o_part = p.o_part;
+  c.lse_part = p.lse_part;
+  c.n_pieces = p.n_pieces;
+  c.out = out;
+  c.lse = lse;
+  c.rows = static_cast<long long>(desc->batch) * desc->q_tokens * desc->q_heads;
+  c.num_splits = hp.num_slots;
+  c.out_fp32 = p.out_fp32;
+  c.nq = desc->q_tokens;
+  c.Hq = desc->q_heads;
+  c.G = p.G;
+  c.kv_heads = desc->kv_heads;
+  return launch_combine(c, desc->head_dim, s);
+}
+
+gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* seqlens, int num_splits, float* o_part, float* lse_part,
+                                void* stream) {
+  gqa_status_t rc = check_desc(desc);
+  if (rc != GQA_OK) return rc;
+  if (num_splits < 1 || num_splits > GQA_MAX_SPLITS) return GQA_ERR_INVALID_ARG;
+  if (desc->batch == 0) return GQA_OK;
+  if ((rc = check_inputs(q, k_cache, v_cache, seqlens)) != GQA_OK) return rc;
+  if (o_part == nullptr || lse_part == nullptr || !aligned(o_part, 16) || !aligned(lse_part, 4))
+    return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  if ((rc = current_device(&dev, &st)) != GQA_OK) return rc;
+  const HostPlan hp = make_plan(desc, num_splits, st->sm_count, true);
+  DecodeParams p;
+  if ((rc = prepare_decode(desc, q, k_cache, v_cache, seqlens, hp, &p)) != GQA_OK) return rc;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  return launch_decode(st, p, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_decode_combine(const float* o_part, const float* lse_part, int num_splits, int64_t rows,
+                                int head_dim, void* out, int out_dtype, float* lse, void* stream) {
+  if (num_splits < 1 || num_splits > GQA_MAX_SPLITS || rows < 0) return GQA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return GQA_ERR_UNSUPPORTED;
+  if (out_dtype != GQA_DTYPE_BF16 && out_dtype != GQA_DTYPE_FP32) return GQA_ERR_INVALID_ARG;
+  if (rows == 0) return GQA_OK;
+  if (o_part == nullptr || lse_part == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(out, 16) || (lse != nullptr && !aligned(lse, 4)))
+    return GQA_ERR_INVALID_ARG;
+  CombineParams c;
+  std::memset(&c, 0, sizeof c);
+  c.o_part = o_part;
+  c.lse_part = lse_part;
+  c.out = out;
+  c.lse = lse;
+  c.rows = rows;
+  c.num_splits = num_splits;
+  c.out_fp32 = out_dtype == GQA_DTYPE_FP32;
+  c.nq = c.Hq = c.G = c.kv_heads = 1;
+  return launch_combine(c, head_dim, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_decode_get_error(int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpyFromSymbol(&bits, g_gqa_error_bits, sizeof bits) != cudaSuccess) return GQA_ERR_CUDA;
+  if (clear && bits != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_gqa_error_bits, &zero, sizeof zero) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  if (bits & kErrTimeout) return GQA_ERR_TIMEOUT;
+  if (bits & kErrBadSeqlen) return GQA_ERR_BAD_SEQLEN;
+  return GQA_OK;
+}
+
+const char* gqa_status_string(gqa_status_t status) {
+  switch (status) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported shape";
+    case GQA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case GQA_ERR_CUDA: return "CUDA runtime error";
+    case GQA_ERR_TIMEOUT: return "a kernel wait timed out";
+    case GQA_ERR_BAD_SEQLEN: return "sequence length out of range (clamped)";
+  }
+  return "unknown status";
+}
+
+gqa_status_t gqa_decode_plan(const gqa_desc_t* desc, const int32_t* seqlens_host, int num_splits, int sm_count,
+                             int* num_ctas, int* plan_mode, int* num_slots, int32_t* items, int64_t max_items,
+                             int64_t* num_items) {
+  gqa_status_t rc = check_desc(desc);
+  if (rc != GQA_OK) return rc;
+  if (num_splits < 0 || num_splits > GQA_MAX_SPLITS) return GQA_ERR_INVALID_ARG;
+  if (desc->batch > 0 && seqlens_host == nullptr) return GQA_ERR_INVALID_ARG;
+  if (sm_count <= 0) {
+    int dev = 0;
+    DeviceState* st = nullptr;
+    if ((rc = current_device(&dev, &st)) != GQA_OK) return rc;
+    sm_count = st->sm_count;
+  }
+  const HostPlan hp = make_plan(desc, num_splits, sm_count, false);
+  if (num_ctas) *num_ctas = hp.pp.num_ctas;
+  if (plan_mode) *plan_mode = hp.pp.mode;
+  if (num_slots) *num_slots = hp.combine ? hp.num_slots : 0;
+  const int B = desc->batch;
+  std::vector<int32_t> clamped(static_cast<size_t>(B > 0 ? B : 1)), pre(static_cast<size_t>(B) + 1, 0);
+  for (int b = 0; b < B; ++b) {
+    clamped[b] = clamp_len(seqlens_host[b], desc->max_seqlen);
+    pre[b + 1] = pre[b] + num_blocks(clamped[b]);
+  }
+  int64_t n = 0;
+  if (desc->batch > 0) {
+    for (int c = 0; c < hp.pp.num_ctas; ++c) {
+      WorkIter it;
+      it.init(&hp.pp, seqlens_host, clamped.data(), pre.data(), c);
+      WorkItem w;
+      while (it.next(w)) {
+        if (items != nullptr && n < max_items) {
+          int32_t* r = items + 8 * n;
+          r[0] = c; r[1] = w.b; r[2] = w.h; r[3] = w.blk_begin; r[4] = w.blk_end;
+          r[5] = w.slot; r[6] = w.first_piece; r[7] = w.n_pieces;
+        }
+        ++n;
+      }
+    }
+  }
+  if (num_items) *num_items = n;
+  return GQA_OK;
+}
+
+gqa_status_t gqa_decode_selftest_timeout(unsigned int timeout_us, void* stream) {
+  if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return GQA_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(1000ull * timeout_us);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // extern "C"

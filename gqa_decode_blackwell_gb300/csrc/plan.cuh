@@ -1,0 +1,201 @@
+// Split-KV work planning, shared by the decode kernel, the combine kernel and
+// the host-side plan introspection entry point.
+//
+// A "unit" is one 128-position KV block of one (batch, KV head) pair.  The
+// decode grid is persistent: CTA c walks a deterministic list of work items,
+// each a contiguous block range [blk_begin, blk_end) of one pair, writing
+// either the final output (the item is the whole pair) or a partial
+// (O_s, lse_s) into workspace slot `slot`.  Splitting the KV length so that a
+// small batch fills the GPU, and merging the partials by log-sum-exp, follows
+// "Building a Faster GQA Decode Kernel for Blackwell SM100", section
+// "Combining the KV splits".  The two partitions below are this library's
+// own (the page leaves its split heuristic unstated).
+//
+//  * PLAN_SPLITS: sequence b is cut into splits_b = clamp(ceil(nblk_b /
+//    min_blocks), 1, S) contiguous block ranges; split s covers blocks
+//    [s*nblk_b/splits_b, (s+1)*nblk_b/splits_b).  Items (b, h, s) are dealt
+//    round-robin to the CTAs.  Splits s >= splits_b are empty items that only
+//    publish lse = -inf.
+//  * PLAN_BALANCED: the U units of all pairs, ordered (b, h, block), are cut
+//    into C' = min(C, U) equal contiguous ranges, one per CTA (CTA c < C'
+//    owns units [floor(cU/C'), floor((c+1)U/C')), at least one each; CTAs
+//    c >= C' own nothing).  Because no range is empty, the CTAs touching a
+//    pair are consecutive.  A pair that falls inside one CTA is
+//    written as final output; a pair cut by CTA boundaries gets one partial
+//    per CTA touching it, in slot (c - first CTA of the pair), and the CTA
+//    that holds its first unit publishes the piece count for the combine.
+//    Pairs of empty sequences belong to the CTA whose range contains their
+//    (zero-length) start; trailing ones to CTA C' - 1.
+#pragma once
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define GQA_HD __host__ __device__ __forceinline__
+#else
+#define GQA_HD inline
+#endif
+
+namespace gqa {
+
+constexpr int kBlockN = 128;  // KV positions per block (the MMA M dimension)
+
+enum PlanMode : int { PLAN_SPLITS = 0, PLAN_BALANCED = 1 };
+
+struct PlanParams {
+  int mode;           // PlanMode
+  int batch;          // B
+  int kv_heads;       // Hkv
+  int max_seqlen;     // S_max: lengths are clamped to [0, S_max]
+  int num_splits;     // PLAN_SPLITS: S
+  int min_blocks;     // PLAN_SPLITS: minimum blocks per split
+  int force_partial;  // PLAN_SPLITS: write partials even when S == 1
+  int num_ctas;       // C: CTAs of the persistent grid
+};
+
+struct WorkItem {
+  int b, h;
+  int L;            // clamped sequence length
+  int blk_begin;    // first KV block (inclusive)
+  int blk_end;      // last KV block (exclusive); begin == end: empty item
+  int slot;         // partial slot, or -1 for final output
+  int first_piece;  // publishes the pair's piece count (PLAN_BALANCED)
+  int n_pieces;     // pieces of this pair (PLAN_BALANCED) / splits of this sequence
+};
+
+GQA_HD int clamp_len(int L, int s_max) { return L < 0 ? 0 : (L > s_max ? s_max : L); }
+GQA_HD int num_blocks(int L) { return (L + kBlockN - 1) / kBlockN; }
+
+// CTA owning unit u under the balanced partition of U units over C CTAs:
+// the largest c with floor(c*U/C) <= u.
+GQA_HD int balanced_cta_of(long long u, long long U, int C) {
+  return static_cast<int>(((u + 1) * static_cast<long long>(C) - 1) / U);
+}
+
+// Round-robin over split items.  `lens` holds raw lengths (clamped here).
+struct SplitIter {
+  const PlanParams* pp;
+  const int32_t* lens;
+  long long w, total;
+  int cta;
+
+  GQA_HD void init(const PlanParams* p, const int32_t* l, int c) {
+    pp = p; lens = l; cta = c; w = c;
+    total = static_cast<long long>(p->batch) * p->kv_heads * p->num_splits;
+  }
+  GQA_HD bool next(WorkItem& it) {
+    if (w >= total) return false;
+    const int S = pp->num_splits;
+    const int s = static_cast<int>(w % S);
+    const long long pair = w / S;
+    it.h = static_cast<int>(pair % pp->kv_heads);
+    it.b = static_cast<int>(pair / pp->kv_heads);
+    it.L = clamp_len(lens[it.b], pp->max_seqlen);
+    const int nblk = num_blocks(it.L);
+    int splits = (nblk + pp->min_blocks - 1) / pp->min_blocks;
+    splits = splits < 1 ? 1 : (splits > S ? S : splits);
+    if (s < splits) {
+      it.blk_begin = static_cast<int>(static_cast<long long>(s) * nblk / splits);
+      it.blk_end = static_cast<int>(static_cast<long long>(s + 1) * nblk / splits);
+    } else {
+      it.blk_begin = it.blk_end = 0;
+    }
+    it.slot = (S == 1 && !pp->force_partial) ? -1 : s;
+    it.first_piece = (s == 0);
+    it.n_pieces = splits;
+    w += pp->num_ctas;
+    return true;
+  }
+};
+
+// Contiguous equal ranges of units.  `lens` are clamped lengths and `pre` the
+// exclusive prefix sums of their block counts (B + 1 entries).
+struct BalancedIter {
+  const PlanParams* pp;
+  const int32_t* lens;
+  const int32_t* pre;
+  long long U, lo, hi;
+  int b, h, cta, C;  // C: effective CTA count min(num_ctas, U), at least 1
+
+  GQA_HD void init(const PlanParams* p, const int32_t* l, const int32_t* prefix, int c) {
+    pp = p; lens = l; pre = prefix; cta = c;
+    const int B = p->batch, H = p->kv_heads;
+    U = static_cast<long long>(H) * pre[B];
+    C = U <= 0 ? 1 : (U < p->num_ctas ? static_cast<int>(U) : p->num_ctas);
+    if (c >= C) {  // this CTA owns nothing
+      b = B; h = 0; lo = hi = U;
+      return;
+    }
+    lo = static_cast<long long>(c) * U / C;
+    hi = static_cast<long long>(c + 1) * U / C;
+    // first pair: smallest b whose units end after lo, or that starts at or after lo
+    int a = 0, z = B;
+    while (a < z) {
+      const int mid = (a + z) / 2;
+      const bool ok = static_cast<long long>(H) * pre[mid + 1] > lo ||
+                      static_cast<long long>(H) * pre[mid] >= lo;
+      if (ok) z = mid; else a = mid + 1;
+    }
+    b = a;
+    h = 0;
+    if (b < B) {
+      const long long start = static_cast<long long>(H) * pre[b];
+      const int nblk = pre[b + 1] - pre[b];
+      if (start < lo && nblk > 0) h = static_cast<int>((lo - start) / nblk);
+    }
+  }
+  GQA_HD void advance() {
+    if (++h == pp->kv_heads) { h = 0; ++b; }
+  }
+  GQA_HD bool next(WorkItem& it) {
+    const int B = pp->batch, H = pp->kv_heads;
+    while (b < B) {
+      const int nblk = pre[b + 1] - pre[b];
+      const long long u_first = static_cast<long long>(H) * pre[b] + static_cast<long long>(h) * nblk;
+      const long long u_end = u_first + nblk;
+      if (nblk == 0) {
+        const bool owned = (u_first >= lo && u_first < hi) || (u_first == U && cta == C - 1);
+        if (!owned) {
+          if (u_first >= hi) return false;
+          advance();
+          continue;
+        }
+        it.b = b; it.h = h; it.L = lens[b];
+        it.blk_begin = it.blk_end = 0;
+        it.slot = -1; it.first_piece = 1; it.n_pieces = 1;
+        advance();
+        return true;
+      }
+      if (u_first >= hi) return false;
+      const long long pl = u_first > lo ? u_first : lo;
+      const long long ph = u_end < hi ? u_end : hi;
+      if (pl >= ph) { advance(); continue; }
+      const int c_first = balanced_cta_of(u_first, U, C);
+      const int c_last = balanced_cta_of(u_end - 1, U, C);
+      it.b = b; it.h = h; it.L = lens[b];
+      it.blk_begin = static_cast<int>(pl - u_first);
+      it.blk_end = static_cast<int>(ph - u_first);
+      it.n_pieces = c_last - c_first + 1;
+      it.slot = it.n_pieces == 1 ? -1 : cta - c_first;
+      it.first_piece = (pl == u_first);
+      advance();
+      return true;
+    }
+    return false;
+  }
+};
+
+// Either iterator behind one interface (the mode is uniform per launch).
+struct WorkIter {
+  SplitIter s;
+  BalancedIter bal;
+  int mode;
+  GQA_HD void init(const PlanParams* p, const int32_t* raw_lens, const int32_t* clamped_lens,
+                   const int32_t* prefix, int cta) {
+    mode = p->mode;
+    if (mode == PLAN_BALANCED) bal.init(p, clamped_lens, prefix, cta);
+    else s.init(p, raw_lens, cta);
+  }
+  GQA_HD bool next(WorkItem& it) { return mode == PLAN_BALANCED ? bal.next(it) : s.next(it); }
+};
+
+}  // namespace gqa

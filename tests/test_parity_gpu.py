@@ -1,0 +1,254 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the fp64
+oracle on the same seeded inputs.
+
+Tolerances: max |O_gpu - O_oracle| <= 2e-2 (bf16 or fp32 output) and
+max |lse_gpu - lse_oracle| <= 1e-3, with -inf LSEs matching exactly.
+"""
+import functools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_blackwell_gb300 as g
+import oracle
+from gqa_decode_blackwell_gb300 import build as gbuild
+from gqa_decode_blackwell_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 2e-2
+LSE_TOL = 1e-3
+DEV = torch.device("cuda:0")
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gbuild.build()
+    g.gqa_decode_get_error(clear=True)
+    yield
+    assert g.gqa_decode_get_error(clear=True) in (g.GQA_OK,)
+
+
+def assert_close(out, lse, ref_out, ref_lse, what=""):
+    o = out.detach().double().cpu().numpy()
+    l = lse.detach().double().cpu().numpy()
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    inf_ref = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(l), inf_ref), f"{what}: -inf LSE pattern differs"
+    err_o = float(np.abs(o - ref_out).max()) if o.size else 0.0
+    err_l = float(np.abs(l[~inf_ref] - ref_lse[~inf_ref]).max()) if (~inf_ref).any() else 0.0
+    assert err_o <= OUT_TOL and err_l <= LSE_TOL, f"{what}: max|dO| {err_o:.3e}, max|dlse| {err_l:.3e}"
+    return err_o, err_l
+
+
+def run_gpu(inp, splits, out_dtype=torch.bfloat16, causal=False, scale=0.0):
+    d = inp if inp.q.is_cuda else inp.to(DEV)
+    out, lse = g.decode(d.q, d.k_cache, d.v_cache, d.seqlens, num_splits=splits, causal=causal, scale=scale,
+                        out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert g.gqa_decode_get_error(clear=True) == g.GQA_OK
+    return out, lse
+
+
+@functools.lru_cache(maxsize=2)
+def config_case(name):
+    cfg = workloads.CONFIGS[name]
+    inp = workloads.make_inputs(cfg)
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, causal=cfg.causal)
+    return cfg, inp.to(DEV), ref
+
+
+FULL = [("tiny", 1), ("tiny", 4), ("tiny", 0), ("llama8b", 0), ("llama8b", 1), ("llama8b", 16),
+        ("llama70b", 8), ("llama70b", 0), ("spec", 0), ("spec", 1), ("spec", 5), ("ragged", 0), ("ragged", 8)]
+
+
+@pytest.mark.parametrize("name,splits", FULL, ids=[f"{n}-s{s}" for n, s in FULL])
+def test_config_full_size(name, splits):
+    """Every element of every config at full size (the oracle is C, fp64, threaded)."""
+    cfg, inp, (ref_out, ref_lse) = config_case(name)
+    out_dtype = torch.float32 if cfg.out_dtype == "fp32" else torch.bfloat16
+    out, lse = run_gpu(inp, splits, out_dtype, cfg.causal)
+    assert_close(out, lse, ref_out, ref_lse, f"{name} splits={splits}")
+
+
+def _nan_tail_inputs(lens, s_max, nq, Hq, Hkv, d, seed):
+    gen = torch.Generator().manual_seed(seed)
+    B = len(lens)
+    q = torch.randn(B, nq, Hq, d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, s_max, Hkv, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, s_max, Hkv, d, generator=gen).to(torch.bfloat16)
+    for b, L in enumerate(lens):   # cache positions past the sequence hold NaN
+        k[b, max(L, 0):] = float("nan")
+        v[b, max(L, 0):] = float("nan")
+    return q, k, v, torch.tensor(lens, dtype=torch.int32)
+
+
+EDGE = [(64, 4, 1, False), (64, 8, 4, True), (128, 4, 1, False), (128, 8, 1, False), (128, 8, 4, True),
+        (128, 16, 2, True), (64, 2, 1, False)]
+
+
+@pytest.mark.parametrize("d,G,nq,causal", EDGE, ids=[f"d{a}-G{b}-nq{c}-{'c' if e else 'n'}" for a, b, c, e in EDGE])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_edge_lengths_and_poisoned_tail(d, G, nq, causal, splits):
+    """Lengths 1, 127, 128, 129, 4097 and 0; every cache position past a
+    sequence's end is NaN, so any read of it (or 0 * NaN) would show."""
+    lens = [1, 127, 128, 129, 4097, 0, nq]
+    Hkv = 2
+    q, k, v, sl = _nan_tail_inputs(lens, 4200, nq, G * Hkv, Hkv, d, seed=100 + d + G + nq)
+    ref_out, ref_lse = oracle.decode(q, k, v, sl, causal=causal)
+    out, lse = run_gpu(workloads.DecodeInputs(None, q, k, v, sl, 1 / math.sqrt(d)).to(DEV), splits,
+                       torch.float32, causal)
+    assert_close(out, lse, ref_out, ref_lse, f"edge d={d} G={G} nq={nq} causal={causal} splits={splits}")
+
+
+def test_more_splits_than_blocks():
+    q, k, v, sl = _nan_tail_inputs([300, 5, 129], 300, 1, 8, 2, 128, seed=7)
+    ref = oracle.decode(q, k, v, sl)
+    for splits in (16, 64):
+        out, lse = run_gpu(workloads.DecodeInputs(None, q, k, v, sl, 0).to(DEV), splits, torch.bfloat16)
+        assert_close(out, lse, *ref, f"splits={splits}")
+
+
+def test_scale_override_and_bf16_fp32_outputs():
+    cfg = workloads.shrink(workloads.CONFIGS["llama8b"], batch=2, seqlen=700)
+    inp = workloads.make_inputs(cfg)
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, scale=0.3)
+    for dt in (torch.bfloat16, torch.float32):
+        out, lse = run_gpu(inp, 0, dt, scale=0.3)
+        assert_close(out, lse, *ref, f"scale 0.3 {dt}")
+
+
+def test_deterministic_bitwise():
+    cfg, inp, _ = config_case("llama8b")
+    a = run_gpu(inp, 0)
+    b = run_gpu(inp, 0)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_splitkv_partials_then_combine():
+    cfg = workloads.shrink(workloads.CONFIGS["spec"], batch=5, seqlen=1000)
+    inp = workloads.make_inputs(cfg)
+    inp.seqlens[:] = torch.tensor([1000, 513, 4, 129, 257], dtype=torch.int32)
+    S = 3
+    begin, end = oracle.split_ranges(inp.seqlens.tolist(), S)
+    parts = [oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, causal=True, pos_begin=begin[s],
+                           pos_end=end[s]) for s in range(S)]
+    ref_full = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, causal=True)
+    d = inp.to(DEV)
+    B, nq, Hq, D = d.q.shape
+    o_part = torch.full((S, B, nq, Hq, D), float("nan"), device=DEV)
+    lse_part = torch.empty(S, B, nq, Hq, device=DEV)
+    g.gqa_decode_splitkv(d.q, d.k_cache, d.v_cache, d.seqlens, S, o_part, lse_part, causal=True)
+    torch.cuda.synchronize()
+    for s in range(S):
+        ref_o, ref_l = parts[s]
+        valid = ~np.isneginf(ref_l)
+        o = o_part[s].double().cpu().numpy()
+        l = lse_part[s].double().cpu().numpy()
+        assert np.array_equal(np.isneginf(l), ~valid)
+        assert np.abs(o[valid] - ref_o[valid]).max() <= OUT_TOL
+        assert np.abs(l[valid] - ref_l[valid]).max() <= LSE_TOL
+    out = torch.empty(B, nq, Hq, D, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, nq, Hq, device=DEV)
+    g.gqa_decode_combine(o_part, lse_part, out, lse)
+    torch.cuda.synchronize()
+    assert_close(out, lse, *ref_full, "splitkv + combine")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_combine_against_oracle(d, out_dtype):
+    rng = np.random.default_rng(d)
+    S, rows = 7, 300
+    o = rng.standard_normal((S, rows, d)).astype(np.float32)
+    l = (rng.standard_normal((S, rows)) * 3).astype(np.float32)
+    l[rng.random((S, rows)) < 0.3] = -np.inf
+    l[:, :5] = -np.inf                       # rows with no valid split
+    o[np.broadcast_to(np.isneginf(l)[..., None], o.shape)] = np.nan   # must never be read
+    ref_out, ref_lse = oracle.combine(o, l)
+    ref_out = np.nan_to_num(ref_out)
+    out = torch.empty(rows, d, dtype=out_dtype, device=DEV)
+    lse = torch.empty(rows, device=DEV)
+    g.gqa_decode_combine(torch.from_numpy(o).to(DEV), torch.from_numpy(l).to(DEV), out, lse)
+    torch.cuda.synchronize()
+    assert_close(out, lse, ref_out, ref_lse, "combine")
+
+
+def test_head_map_golden_on_gpu():
+    with open(os.path.join(GOLDEN, "gqa_head_groups.json")) as f:
+        gold = json.load(f)
+    for ex in gold["examples"]:
+        Hq, Hkv = ex["num_qo_heads"], ex["num_kv_heads"]
+        if Hq // Hkv > 32:
+            continue
+        gen = torch.Generator().manual_seed(3)
+        q = torch.randn(1, 1, Hq, 128, generator=gen).to(torch.bfloat16)
+        k = torch.randn(1, 200, Hkv, 128, generator=gen).to(torch.bfloat16)
+        v = torch.arange(1, Hkv + 1, dtype=torch.float32).view(1, 1, Hkv, 1).expand(1, 200, Hkv, 128)
+        v = v.contiguous().to(torch.bfloat16)
+        out, _ = run_gpu(workloads.DecodeInputs(None, q, k, v, torch.tensor([200], dtype=torch.int32), 0), 0,
+                         torch.float32)
+        got = [int(round(float(out[0, 0, hq, 0]))) - 1 for hq in range(Hq)]
+        assert got == ex["kv_head_of_q_head"]
+
+
+def test_graph_capture_and_replay():
+    cfg = workloads.shrink(workloads.CONFIGS["llama8b"], batch=4, seqlen=1500)
+    a = workloads.make_inputs(cfg).to(DEV)
+    b = workloads.make_inputs(cfg, seed=99)
+    ref_b = oracle.decode(b.q, b.k_cache, b.v_cache, b.seqlens)
+    out = torch.empty(a.q.shape, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(a.q.shape[:3], device=DEV)
+    ws_bytes = g.gqa_decode_workspace_size(a.q, a.k_cache, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    g.gqa_decode_attn(a.q, a.k_cache, a.v_cache, a.seqlens, out, lse, 0, ws)   # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.gqa_decode_attn(a.q, a.k_cache, a.v_cache, a.seqlens, out, lse, 0, ws)
+    a.q.copy_(b.q); a.k_cache.copy_(b.k_cache); a.v_cache.copy_(b.v_cache); a.seqlens.copy_(b.seqlens)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert_close(out, lse, *ref_b, "graph replay")
+
+
+def test_bad_seqlen_is_clamped_and_flagged():
+    q, k, v, sl = _nan_tail_inputs([50, 90], 100, 1, 4, 1, 64, seed=5)
+    k[:] = torch.randn(k.shape).to(torch.bfloat16)
+    v[:] = torch.randn(v.shape).to(torch.bfloat16)
+    bad = torch.tensor([500, -3], dtype=torch.int32)
+    ref = oracle.decode(q, k, v, [100, 0])
+    d = workloads.DecodeInputs(None, q, k, v, bad, 0).to(DEV)
+    out, lse = g.decode(d.q, d.k_cache, d.v_cache, d.seqlens, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert g.gqa_decode_get_error(clear=True) == g.GQA_ERR_BAD_SEQLEN
+    assert_close(out, lse, *ref, "clamped lengths")
+
+
+def test_timeout_selftest_reports_and_context_survives():
+    """A bounded wait on a barrier nothing completes returns an error status;
+    the context stays usable for the next decode."""
+    g.gqa_decode_selftest_timeout(20000)
+    assert g.gqa_decode_get_error(clear=True) == g.GQA_ERR_TIMEOUT
+    assert g.gqa_decode_get_error(clear=True) == g.GQA_OK
+    cfg, inp, ref = config_case("tiny")
+    out, lse = run_gpu(inp, 4, torch.float32)
+    assert_close(out, lse, *ref, "after timeout")
+
+
+def test_empty_batch():
+    q = torch.empty(0, 1, 8, 128, dtype=torch.bfloat16, device=DEV)
+    k = torch.empty(0, 16, 2, 128, dtype=torch.bfloat16, device=DEV)
+    sl = torch.empty(0, dtype=torch.int32, device=DEV)
+    out = torch.empty(0, 1, 8, 128, dtype=torch.bfloat16, device=DEV)
+    g.gqa_decode_attn(q, k, k, sl, out)
+    torch.cuda.synchronize()

@@ -1,0 +1,130 @@
+"""Host-side planning: the work decomposition the decode kernel walks
+(plan.cuh, enumerated through gqa_decode_plan) covers every KV block of every
+(batch, KV head) pair exactly once, with consistent partial slots and piece
+counts (CPU only)."""
+import collections
+
+import numpy as np
+import pytest
+
+import gqa_decode_blackwell_gb300 as g
+import oracle
+from gqa_decode_blackwell_gb300 import build as gbuild
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gbuild.build()
+
+
+def _desc(B, Hkv, s_max, G=4, nq=1, d=128):
+    return g.gqa_desc_t(B, nq, Hkv * G, Hkv, d, s_max, 0.0, 0, 0)
+
+
+def _blocks(L):
+    return (max(L, 0) + 127) // 128
+
+
+def check_balanced(seqlens, Hkv, s_max, sm):
+    desc = _desc(len(seqlens), Hkv, s_max)
+    C, mode, slots, items = g.gqa_decode_plan(desc, seqlens, 0, sm)
+    assert mode == 1
+    lens = [min(max(int(L), 0), s_max) for L in seqlens]
+    U = sum(_blocks(L) for L in lens) * Hkv
+    assert C == max(1, min(sm, len(lens) * Hkv * _blocks(s_max)))
+    C_eff = max(1, min(C, U))
+    cover = collections.Counter()
+    per_pair = collections.defaultdict(list)
+    per_cta = collections.Counter()
+    for c, b, h, b0, b1, slot, first, npieces in items:
+        per_pair[(b, h)].append((c, b0, b1, slot, first, npieces))
+        per_cta[c] += b1 - b0
+        for blk in range(b0, b1):
+            cover[(b, h, blk)] += 1
+    # every unit exactly once
+    expect = {(b, h, k) for b, L in enumerate(lens) for h in range(Hkv) for k in range(_blocks(L))}
+    assert set(cover) == expect and all(v == 1 for v in cover.values())
+    # every pair visited, pieces consistent
+    for b, L in enumerate(lens):
+        for h in range(Hkv):
+            pieces = per_pair[(b, h)]
+            assert len(pieces) >= 1
+            n = len(pieces)
+            assert all(p[5] == n for p in pieces)
+            assert sum(p[4] for p in pieces) == 1
+            if n == 1:
+                assert pieces[0][3] == -1
+            else:
+                assert sorted(p[3] for p in pieces) == list(range(n))
+                assert n <= slots
+            # pieces are contiguous and in CTA order
+            ordered = sorted(pieces)
+            assert ordered[0][1] == 0 and ordered[-1][2] == _blocks(L)
+            for a, z in zip(ordered, ordered[1:]):
+                assert a[2] == z[1]
+    # only the first C_eff CTAs work; their loads differ by at most one block
+    assert all(c < C_eff for c in per_cta)
+    loads = [per_cta.get(c, 0) for c in range(C_eff)]
+    if U > 0:
+        assert max(loads) - min(loads) <= 1
+        assert sum(loads) == U
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_balanced_plan_random(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 40))
+    Hkv = int(rng.choice([1, 2, 8]))
+    s_max = int(rng.integers(1, 5000))
+    lens = rng.integers(-5, s_max + 1, size=B)
+    lens[rng.random(B) < 0.2] = 0
+    sm = int(rng.choice([1, 3, 16, 152]))
+    check_balanced(lens.tolist(), Hkv, s_max, sm)
+    # the same lengths in a much larger cache: fewer units than CTAs
+    check_balanced(lens.tolist(), Hkv, s_max * 7, 152)
+
+
+@pytest.mark.parametrize("lens,Hkv,s_max,sm", [
+    ([0, 0, 0], 2, 128, 152),         # nothing to read: every pair is an empty item
+    ([200], 2, 4200, 152),            # fewer units than CTAs, pairs cut in two
+    ([129], 1, 4200, 152),
+    ([1, 127, 128, 129, 4097, 0, 1], 2, 4200, 152),
+    ([5000, 0, 3], 1, 5000, 16),
+    ([1], 1, 1, 152),                 # one unit, one CTA
+    ([512], 1, 512, 152),             # tiny config: 4 units
+    ([4096] * 8, 8, 4096, 152),       # Llama-8B-shaped
+    ([8192] * 16, 8, 8192, 152),      # 70B-shaped
+    ([2048] * 32, 2, 2048, 152),      # speculative
+    ([131072, 1024, 70000, 0], 8, 131072, 152),
+    ([0, 300, 0, 0, 129, 0], 3, 300, 5),
+])
+def test_balanced_plan_cases(lens, Hkv, s_max, sm):
+    check_balanced(lens, Hkv, s_max, sm)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 64])
+def test_split_plan_matches_documented_partition(S):
+    rng = np.random.default_rng(S)
+    B, Hkv, s_max = 6, 2, 1000
+    lens = rng.integers(0, s_max + 1, size=B).tolist()
+    lens[0] = 1
+    desc = _desc(B, Hkv, s_max)
+    C, mode, slots, items = g.gqa_decode_plan(desc, lens, S, 152)
+    assert mode == 0 and C == min(152, B * Hkv * S)
+    begin, end = oracle.split_ranges(lens, S, block=128)
+    seen = set()
+    for c, b, h, b0, b1, slot, first, npieces in items:
+        w = (b * Hkv + h) * S + (slot if slot >= 0 else 0)
+        assert w % C == c
+        s = slot if slot >= 0 else 0
+        assert (S == 1) == (slot == -1)
+        assert min(b0 * 128, lens[b]) == begin[s, b] or b0 == b1
+        assert min(b1 * 128, lens[b]) == end[s, b]
+        seen.add((b, h, s))
+    assert len(seen) == B * Hkv * S
+
+
+def test_auto_falls_back_to_splits_for_huge_batches():
+    lens = [300] * 1500
+    C, mode, slots, items = g.gqa_decode_plan(_desc(1500, 1, 300), lens, 0, 152)
+    assert mode == 0
