@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""GQA decode benchmark on GB300: one JSON line on rank 0.
+
+A step is one gqa_decode_attn call (split-KV decode kernel + LSE combine)
+over one batch of seeded synthetic input already resident in HBM.  Steps
+cycle through a rotating pool of distinct KV caches larger than L2 and are
+replayed from CUDA graphs of back-to-back calls.  Defaults: the Llama-8B
+shaped workload (B8, 32/8 heads, d128, L4096, bf16), automatic splitting,
+one GPU.  With torchrun, every rank runs an independent replica (the work
+does not shard with an exchange step) and the slowest rank's time is used.
+
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gqa_decode_blackwell_gb300 import workloads  # noqa: E402
+
+METRIC = "decode attn µs/call & achieved KV-read HBM GB/s (fraction of GB300 peak)"
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["decode_kernel.cuh", "sm103_ptx.cuh", "plan.cuh"]
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity for one process)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gqa_decode_blackwell_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    path = os.path.join(PROFILES, f"decode_kernel_{workload}.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None, "no ncu summary for this workload"
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256") != kernel_source_digest():
+        return None, "kernel changed since the ncu capture"
+    try:
+        return float(fields["dram_bytes_per_launch"]), path
+    except (KeyError, ValueError):
+        return None, "summary has no dram_bytes_per_launch"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ["uuid", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.window = None
+        self.proc = None
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            pass
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = [s for t, s in self.samples if len(s) == len(self.FIELDS)]
+        if self.uuid:
+            mine = [s for s in rows if self.uuid.replace("GPU-", "") in s[0]]
+            rows = mine or rows
+        t0, t1 = self.window or (0, float("inf"))
+        inside = [s for (t, s) in self.samples if t0 - 0.25 <= t <= t1 + 0.25 and s in rows]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in use for i in range(4) if s[4 + i].lower().startswith("active")})
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[1]) for s in use if num(s[1]) is not None]
+        mx = [num(s[2]) for s in use if num(s[2]) is not None]
+        pw = [num(s[3]) for s in use if num(s[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------- our kernels
+class GraphSteps:
+    """Runs n decode calls as replays of CUDA graphs of `per` back-to-back calls."""
+
+    def __init__(self, call, per: int, stream):
+        self.call, self.per, self.stream = call, per, stream
+        self.graphs = {}
+
+    def _graph(self, n):
+        if n not in self.graphs:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(gr, stream=self.stream):
+                    for j in range(n):
+                        self.call(j)
+            self.graphs[n] = gr
+        return self.graphs[n]
+
+    def run(self, n: int):
+        full, rem = divmod(n, self.per)
+        if full:
+            gf = self._graph(self.per)
+            for _ in range(full):
+                gf.replay()
+        if rem:
+            self._graph(rem).replay()
+
+
+def bench_ours(args, cfg, world, rank, local):
+    import gqa_decode_blackwell_gb300 as g
+    from gqa_decode_blackwell_gb300 import build as gbuild
+
+    gbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    splits = args.splits
+    out_dtype = torch.float32 if cfg.out_dtype == "fp32" else torch.bfloat16
+    host = workloads.make_inputs(cfg)
+    kv_bytes = host.kv_bytes()
+    alloc_bytes = host.k_cache.numel() * 2 * 2
+    pool = max(2, math.ceil(args.pool_mb * 2**20 / alloc_bytes) + 1)
+    base = host.to(dev)
+    copies = [base] + [workloads.DecodeInputs(cfg, base.q.clone(), base.k_cache.clone(), base.v_cache.clone(),
+                                              base.seqlens.clone(), base.scale) for _ in range(pool - 1)]
+    out = torch.empty(base.q.shape, dtype=out_dtype, device=dev)
+    lse = torch.empty(base.q.shape[:3], dtype=torch.float32, device=dev)
+    ws_bytes = g.gqa_decode_workspace_size(base.q, base.k_cache, splits, causal=cfg.causal, out_dtype=out_dtype)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    nc, mode, slots, _ = g.gqa_decode_plan(g.make_desc(base.q, base.k_cache, causal=cfg.causal, out_dtype=out_dtype),
+                                           host.seqlens.tolist(), splits, 0, max_items=1)
+    launches_per_step = 1 + (1 if slots > 0 else 0)
+
+    def attn(j):
+        c = copies[j % pool]
+        g.gqa_decode_attn(c.q, c.k_cache, c.v_cache, c.seqlens, out, lse, splits, ws, causal=cfg.causal)
+
+    def split_only(j):
+        c = copies[j % pool]
+        g.gqa_decode_attn_split(c.q, c.k_cache, c.v_cache, c.seqlens, out, lse, splits, ws, causal=cfg.causal)
+
+    stream = torch.cuda.Stream(device=dev)
+    for j in range(pool):  # eager once per copy: kernel attributes, tensor maps
+        attn(j)
+    torch.cuda.synchronize()
+    if g.gqa_decode_get_error(clear=True) != g.GQA_OK:
+        raise RuntimeError("decode reported a device error during warm-up")
+    steps = GraphSteps(attn, pool, stream)
+    dec_steps = GraphSteps(split_only, pool, stream)
+    steps.run(pool)
+    dec_steps.run(pool)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.6)
+    cur = torch.cuda.current_stream(dev)
+    steps.run(args.warmup)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(cur)
+    steps.run(args.steps)
+    ev1.record(cur)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world, dev)
+    if clocks:
+        clocks.mark(t0, t1)
+    ms_step = ev0.elapsed_time(ev1) / args.steps
+    ms_step_max = reduce_max(ms_step, world, dev)
+
+    # decode kernel alone (same plan, same launches), for the roofline
+    dec_n = args.steps
+    dec_steps.run(min(args.warmup, pool))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    dec_steps.run(dec_n)
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms_decode = e0.elapsed_time(e1) / dec_n
+    if clocks:
+        clocks.stop()
+    if g.gqa_decode_get_error(clear=True) != g.GQA_OK:
+        raise RuntimeError("decode reported a device error in the timed region")
+
+    # end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h = [host.q.pin_memory(), host.k_cache.pin_memory(), host.v_cache.pin_memory(), host.seqlens.pin_memory()]
+        d = [torch.empty_like(x, device=dev) for x in h]
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in h)
+        d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+        def e2e_step():
+            for dst, src in zip(d, h):
+                dst.copy_(src, non_blocking=True)
+            g.gqa_decode_attn(d[0], d[1], d[2], d[3], out, lse, splits, ws, causal=cfg.causal)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world, dev)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(cur)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        a1.record(cur)
+        torch.cuda.synchronize()
+        ms_e2e = reduce_max(a0.elapsed_time(a1) / args.e2e_steps, world, dev)
+        e2e = {"value": round(world * kv_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(ms_e2e, 4), "steps": args.e2e_steps, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    peak, peak_kind = measured_peak()
+    achieved = kv_bytes / (ms_decode * 1e-3) / 1e9
+    traffic, traffic_src = ncu_traffic(cfg.name)
+    roofline = {"bound": "hbm", "kernel": "gqa_decode_kernel", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": traffic, "traffic_source": traffic_src, "us_per_launch": round(ms_decode * 1e3, 3),
+                "algorithmic_bytes_per_launch": kv_bytes}
+    value = world * kv_bytes / (ms_step_max * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(host, cfg, args.cpu_seconds)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5), "us_per_call": round(ms_step_max * 1e3, 3),
+        "frac_of_peak": round(value / world / peak, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic: seeded randn rounded to bf16",
+        "config": {"workload": cfg.name, "description": cfg.description, "batch": cfg.batch,
+                   "q_tokens": cfg.q_tokens, "q_heads": cfg.q_heads, "kv_heads": cfg.kv_heads,
+                   "head_dim": cfg.head_dim, "seqlen": cfg.seqlen if cfg.ragged is None else "ragged",
+                   "seqlens_sum": int(host.seqlens.sum().item()), "kv_bytes_per_step": kv_bytes,
+                   "num_splits": "auto" if splits == 0 else splits, "plan": ["splits", "balanced"][mode],
+                   "ctas": nc, "partial_slots": slots,
+                   "l2": f"rotating pool of {pool} KV caches ({pool * alloc_bytes / 1e6:.0f} MB) > 129 MB L2",
+                   "launch": f"CUDA graphs of {pool} back-to-back calls, PDL between kernels",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary() if clocks else None, "e2e": e2e, "cpu_baseline": cpu,
+    }
+    return result
+
+
+def cpu_baseline(host, cfg, seconds):
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    orc = oracle.load()
+    t = time.perf_counter()
+    orc.decode(host.q, host.k_cache, host.v_cache, host.seqlens, causal=cfg.causal, nthreads=cores)
+    one = time.perf_counter() - t
+    reps = max(1, min(1000, int(seconds / max(one, 1e-6))))
+    t = time.perf_counter()
+    for _ in range(reps):
+        orc.decode(host.q, host.k_cache, host.v_cache, host.seqlens, causal=cfg.causal, nthreads=cores)
+    dt = time.perf_counter() - t
+    return {"value": round(reps * host.kv_bytes() / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "sample": f"the whole {cfg.name} workload, {reps} repetitions ({dt:.1f} s)"}
+
+
+# ------------------------------------------------------------ reference arm
+def bench_reference(args, cfg):
+    import oracle
+
+    orc = oracle.load()
+    cores = len(os.sched_getaffinity(0))
+    host = workloads.make_inputs(cfg)
+    B = cfg.batch
+    per_b = [int(L) * cfg.kv_heads * cfg.head_dim * 4 for L in host.seqlens.tolist()]
+
+    def step(i):
+        b = i % B
+        orc.decode(host.q[b:b + 1], host.k_cache[b:b + 1], host.v_cache[b:b + 1], host.seqlens[b:b + 1],
+                   causal=cfg.causal, nthreads=cores)
+        return per_b[b]
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    nbytes = sum(step(i) for i in range(args.steps))
+    dt = time.perf_counter() - t
+    value = nbytes / dt / 1e9
+    sample = f"one sequence (all heads) of the {cfg.name} workload per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded randn rounded to bf16",
+        "config": {"workload": cfg.name, "description": cfg.description, "kv_bytes_per_step_mean": sum(per_b) / B},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama8b", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--splits", type=int, default=None, help="0 = automatic (default: the config's first)")
+    ap.add_argument("--pool-mb", type=float, default=512.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+    cfg = workloads.CONFIGS[args.config]
+    if args.splits is None:
+        args.splits = cfg.num_splits[0]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args, cfg)), flush=True)
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        res = bench_ours(args, cfg, world, rank, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

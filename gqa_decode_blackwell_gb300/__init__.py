@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
             L.gqa_decode_workspace_size.restype = SZ
             L.gqa_decode_attn.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
             L.gqa_decode_attn.restype = I
+            L.gqa_decode_attn_split.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
+            L.gqa_decode_attn_split.restype = I
+            L.gqa_decode_attn_merge.argtypes = [D, P, P, I, P, SZ, P]
+            L.gqa_decode_attn_merge.restype = I
             L.gqa_decode_splitkv.argtypes = [D, P, P, P, P, I, P, P, P]
             L.gqa_decode_splitkv.restype = I
             L.gqa_decode_combine.argtypes = [P, P, I, I64, I, P, I, P, P]
@@ -150,6 +154,28 @@ def gqa_decode_attn(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int
     rc = lib().gqa_decode_attn(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
                                _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "gqa_decode_attn")
+
+
+def gqa_decode_attn_split(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int = 0, workspace=None, *,
+                          scale: float = 0.0, causal: bool = False, stream=None) -> None:
+    """The decode-kernel half of gqa_decode_attn (see the C header)."""
+    _inputs_ok(q, k_cache, v_cache, seqlens)
+    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().gqa_decode_attn_split(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
+                                     _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), ws_bytes,
+                                     _stream(stream))
+    _check(rc, "gqa_decode_attn_split")
+
+
+def gqa_decode_attn_merge(q, k_cache, out, lse=None, num_splits: int = 0, workspace=None, *, causal: bool = False,
+                          stream=None) -> None:
+    """The combine half of gqa_decode_attn over the workspace of gqa_decode_attn_split."""
+    desc = make_desc(q, k_cache, causal=causal, out_dtype=out.dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().gqa_decode_attn_merge(ctypes.byref(desc), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace),
+                                     ws_bytes, _stream(stream))
+    _check(rc, "gqa_decode_attn_merge")
 
 
 def gqa_decode_splitkv(q, k_cache, v_cache, seqlens, num_splits: int, o_part, lse_part, *, scale: float = 0.0,

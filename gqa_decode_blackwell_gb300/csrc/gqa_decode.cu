@@ -316,14 +316,21 @@ size_t gqa_decode_workspace_size(const gqa_desc_t* desc, int num_splits) {
   return ws_layout(desc, hp).total;
 }
 
-gqa_status_t gqa_decode_attn(const gqa_desc_t* desc, const void* q, const void* k_cache, const void* v_cache,
-                             const int32_t* seqlens, void* out, float* lse, int num_splits, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace gqa {
+namespace {
+
+enum AttnPart : int { ATTN_BOTH = 3, ATTN_SPLIT = 1, ATTN_MERGE = 2 };
+
+gqa_status_t attn_impl(const gqa_desc_t* desc, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* seqlens, void* out, float* lse, int num_splits, void* workspace,
+                       size_t workspace_bytes, cudaStream_t s, int parts) {
   gqa_status_t rc = check_desc(desc);
   if (rc != GQA_OK) return rc;
   if (num_splits < 0 || num_splits > GQA_MAX_SPLITS) return GQA_ERR_INVALID_ARG;
   if (desc->batch == 0) return GQA_OK;  // nothing to compute; pointers may be null
-  if ((rc = check_inputs(q, k_cache, v_cache, seqlens)) != GQA_OK) return rc;
+  if ((parts & ATTN_SPLIT) && (rc = check_inputs(q, k_cache, v_cache, seqlens)) != GQA_OK) return rc;
   if (out == nullptr || !aligned(out, 16) || (lse != nullptr && !aligned(lse, 4))) return GQA_ERR_INVALID_ARG;
   int dev = 0;
   DeviceState* st = nullptr;
@@ -332,34 +339,61 @@ gqa_status_t gqa_decode_attn(const gqa_desc_t* desc, const void* q, const void* 
   const WsLayout wl = ws_layout(desc, hp);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total || !aligned(workspace, kWsAlign)))
     return GQA_ERR_WORKSPACE;
-  DecodeParams p;
-  if ((rc = prepare_decode(desc, q, k_cache, v_cache, seqlens, hp, &p)) != GQA_OK) return rc;
-  p.out = out;
-  p.lse = lse;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (hp.combine) {
-    p.o_part = reinterpret_cast<float*>(ws + wl.o_off);
-    p.lse_part = reinterpret_cast<float*>(ws + wl.lse_off);
-    if (hp.use_n_pieces) p.n_pieces = reinterpret_cast<int32_t*>(ws + wl.np_off);
+  float* o_part = hp.combine ? reinterpret_cast<float*>(ws + wl.o_off) : nullptr;
+  float* lse_part = hp.combine ? reinterpret_cast<float*>(ws + wl.lse_off) : nullptr;
+  int32_t* n_pieces = (hp.combine && hp.use_n_pieces) ? reinterpret_cast<int32_t*>(ws + wl.np_off) : nullptr;
+  if (parts & ATTN_SPLIT) {
+    DecodeParams p;
+    if ((rc = prepare_decode(desc, q, k_cache, v_cache, seqlens, hp, &p)) != GQA_OK) return rc;
+    p.out = out;
+    p.lse = lse;
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.n_pieces = n_pieces;
+    if ((rc = launch_decode(st, p, s)) != GQA_OK) return rc;
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((rc = launch_decode(st, p, s)) != GQA_OK) return rc;
-  if (!hp.combine) return GQA_OK;
+  if (!(parts & ATTN_MERGE) || !hp.combine) return GQA_OK;
   CombineParams c;
   std::memset(&c, 0, sizeof c);
-  c.o_part = p.o_part;
-  c.lse_part = p.lse_part;
-  c.n_pieces = p.n_pieces;
+  c.o_part = o_part;
+  c.lse_part = lse_part;
+  c.n_pieces = n_pieces;
   c.out = out;
   c.lse = lse;
   c.rows = static_cast<long long>(desc->batch) * desc->q_tokens * desc->q_heads;
   c.num_splits = hp.num_slots;
-  c.out_fp32 = p.out_fp32;
+  c.out_fp32 = desc->out_dtype == GQA_DTYPE_FP32;
   c.nq = desc->q_tokens;
   c.Hq = desc->q_heads;
-  c.G = p.G;
+  c.G = desc->q_heads / desc->kv_heads;
   c.kv_heads = desc->kv_heads;
   return launch_combine(c, desc->head_dim, s);
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+gqa_status_t gqa_decode_attn(const gqa_desc_t* desc, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* seqlens, void* out, float* lse, int num_splits, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return attn_impl(desc, q, k_cache, v_cache, seqlens, out, lse, num_splits, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), ATTN_BOTH);
+}
+
+gqa_status_t gqa_decode_attn_split(const gqa_desc_t* desc, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* seqlens, void* out, float* lse,
+                                   int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_impl(desc, q, k_cache, v_cache, seqlens, out, lse, num_splits, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), ATTN_SPLIT);
+}
+
+gqa_status_t gqa_decode_attn_merge(const gqa_desc_t* desc, void* out, float* lse, int num_splits, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return attn_impl(desc, nullptr, nullptr, nullptr, nullptr, out, lse, num_splits, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), ATTN_MERGE);
 }
 
 gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const void* k_cache, const void* v_cache,

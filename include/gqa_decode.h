@@ -113,6 +113,23 @@ gqa_status_t gqa_decode_attn(const gqa_desc_t* desc, const void* q, const void* 
                              int num_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The two halves of gqa_decode_attn, for callers that want to run other work
+ * between them or time them apart.  gqa_decode_attn_split runs the
+ * split-KV decode kernel of gqa_decode_attn (same plan, same arguments):
+ * rows whose KV range was not split are final in out / lse, split rows leave
+ * their partials in the workspace.  gqa_decode_attn_merge then runs the
+ * combine kernel of gqa_decode_attn over that workspace (no-op when nothing
+ * was split).  The pair, on one stream, equals one gqa_decode_attn call; the
+ * workspace must not be reused in between.
+ */
+gqa_status_t gqa_decode_attn_split(const gqa_desc_t* desc, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* seqlens, void* out,
+                                   float* lse, int num_splits, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+gqa_status_t gqa_decode_attn_merge(const gqa_desc_t* desc, void* out, float* lse, int num_splits,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The split step alone: for each sequence b the KV blocks are cut into
  * splits_b = min(num_splits, ceil(L_b / 128)) (at least 1) contiguous ranges;
  * split s covers blocks [s*nblk/splits_b, (s+1)*nblk/splits_b) with

@@ -252,3 +252,16 @@ def test_empty_batch():
     out = torch.empty(0, 1, 8, 128, dtype=torch.bfloat16, device=DEV)
     g.gqa_decode_attn(q, k, k, sl, out)
     torch.cuda.synchronize()
+
+
+def test_split_then_merge_equals_attn():
+    cfg, inp, ref = config_case("llama8b")
+    out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(inp.q.shape[:3], device=DEV)
+    ws = torch.empty(g.gqa_decode_workspace_size(inp.q, inp.k_cache, 0), dtype=torch.uint8, device=DEV)
+    g.gqa_decode_attn_split(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, out, lse, 0, ws)
+    g.gqa_decode_attn_merge(inp.q, inp.k_cache, out, lse, 0, ws)
+    torch.cuda.synchronize()
+    assert_close(out, lse, *ref, "split + merge")
+    a_out, a_lse = run_gpu(inp, 0)
+    assert torch.equal(out, a_out) and torch.equal(lse, a_lse)
