@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.gqa_decode_workspace_size.restype = SZ
             L.gqa_decode_attn.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
             L.gqa_decode_attn.restype = I
+            L.gqa_decode_attn_static_workspace.argtypes = [D, P, P, P, P, P, P, I, P]
+            L.gqa_decode_attn_static_workspace.restype = I
             L.gqa_decode_attn_split.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
             L.gqa_decode_attn_split.restype = I
             L.gqa_decode_attn_merge.argtypes = [D, P, P, I, P, SZ, P]
@@ -154,6 +156,18 @@ def gqa_decode_attn(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int
     rc = lib().gqa_decode_attn(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
                                _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "gqa_decode_attn")
+
+
+def gqa_decode_attn_static_workspace(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int = 0, *,
+                                     scale: float = 0.0, causal: bool = False, stream=None) -> None:
+    """gqa_decode_attn using the library's static device workspace instead of a
+    caller-allocated one (for callers that cannot allocate; see the C header)."""
+    _inputs_ok(q, k_cache, v_cache, seqlens)
+    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype)
+    rc = lib().gqa_decode_attn_static_workspace(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                _ptr(seqlens), _ptr(out), _ptr(lse), int(num_splits),
+                                                _stream(stream))
+    _check(rc, "gqa_decode_attn_static_workspace")
 
 
 def gqa_decode_attn_split(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int = 0, workspace=None, *,

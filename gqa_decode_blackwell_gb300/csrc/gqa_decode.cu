@@ -396,6 +396,56 @@ gqa_status_t gqa_decode_attn_merge(const gqa_desc_t* desc, void* out, float* lse
                    static_cast<cudaStream_t>(stream), ATTN_MERGE);
 }
 
+}  // extern "C"
+
+namespace gqa {
+namespace {
+
+// Library-owned workspace for gqa_decode_attn_static_workspace.  It lives in
+// the module's global memory, so every GPU that loads this library holds
+// GQA_STATIC_WORKSPACE_BYTES of it until the process exits.
+static __device__ __align__(256) unsigned char g_static_workspace[GQA_STATIC_WORKSPACE_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_workspace on the current device.  The name of a
+// __device__ array in host code is only a host-side stand-in, so the address
+// is looked up once per device, with that device current.
+gqa_status_t static_workspace_ptr(int dev, void** out) {
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return GQA_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return GQA_OK;
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+gqa_status_t gqa_decode_attn_static_workspace(const gqa_desc_t* desc, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* seqlens, void* out, float* lse,
+                                              int num_splits, void* stream) {
+  gqa_status_t rc = check_desc(desc);
+  if (rc != GQA_OK) return rc;
+  if (num_splits < 0 || num_splits > GQA_MAX_SPLITS) return GQA_ERR_INVALID_ARG;
+  if (desc->batch == 0) return GQA_OK;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  if ((rc = current_device(&dev, &st)) != GQA_OK) return rc;
+  const size_t need = ws_layout(desc, make_plan(desc, num_splits, st->sm_count, false)).total;
+  if (need > GQA_STATIC_WORKSPACE_BYTES) return GQA_ERR_WORKSPACE;  // larger than the static array
+  void* ws = nullptr;
+  if ((rc = static_workspace_ptr(dev, &ws)) != GQA_OK) return rc;
+  return gqa_decode_attn(desc, q, k_cache, v_cache, seqlens, out, lse, num_splits, ws, GQA_STATIC_WORKSPACE_BYTES,
+                         stream);
+}
+
 gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* seqlens, int num_splits, float* o_part, float* lse_part,
                                 void* stream) {

@@ -113,6 +113,34 @@ gqa_status_t gqa_decode_attn(const gqa_desc_t* desc, const void* q, const void* 
                              int num_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gqa_decode_attn without a caller-provided workspace, for callers that
+ * cannot allocate device memory where they call decode: plugins that must
+ * stay inside a host framework's own memory arena, serving runtimes that fix
+ * their memory footprint at start-up and forbid allocation afterwards, and
+ * latency-critical paths that cannot afford cudaMalloc's implicit
+ * device-wide synchronisation.  (The pages describe no such entry point; it
+ * is this library's addition.)
+ *
+ * The split partials go to a workspace owned by the library: a static array
+ * of GQA_STATIC_WORKSPACE_BYTES in device global memory, which every GPU that
+ * loads the library holds until the process exits.  Arguments and results are
+ * those of gqa_decode_attn.  A problem whose workspace
+ * (gqa_decode_workspace_size) exceeds GQA_STATIC_WORKSPACE_BYTES is rejected
+ * with GQA_ERR_WORKSPACE before anything is launched.  The call allocates and
+ * frees nothing.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Every call on a device shares the one
+ * array and nothing in it needs clearing (each call writes every value it
+ * reads), but calls whose kernels overlap on the GPU -- on different streams,
+ * or different host threads -- race on it: order them on one stream.
+ */
+#define GQA_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+gqa_status_t gqa_decode_attn_static_workspace(const gqa_desc_t* desc, const void* q,
+                                              const void* k_cache, const void* v_cache,
+                                              const int32_t* seqlens, void* out, float* lse,
+                                              int num_splits, void* stream);
+
+/*
  * The two halves of gqa_decode_attn, for callers that want to run other work
  * between them or time them apart.  gqa_decode_attn_split runs the
  * split-KV decode kernel of gqa_decode_attn (same plan, same arguments):

@@ -1,0 +1,88 @@
+"""gqa_decode_attn_static_workspace: the decode entry point for callers that
+cannot allocate device memory where they call it (plugins confined to a host
+framework's arena, runtimes with a fixed start-up footprint, paths that cannot
+take cudaMalloc's device-wide synchronisation).  It must give the results of
+gqa_decode_attn with a caller workspace, on consecutive calls that reuse the
+library's one static workspace, and must refuse problems too big for it.
+
+Kept in a file that pytest collects last, so that a run stopping at the first
+failure has already run every other test; it also passes on its own.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_blackwell_gb300 as g
+from gqa_decode_blackwell_gb300 import build as gbuild
+from gqa_decode_blackwell_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 2e-2
+LSE_TOL = 1e-3
+STATIC_BYTES = 32 * 1024 * 1024
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gbuild.build()
+    g.gqa_decode_get_error(clear=True)
+
+
+def _static_call(inp, out, lse, splits, causal):
+    """The new entry point, straight through the C ABI."""
+    desc = g.make_desc(inp.q, inp.k_cache, causal=causal, out_dtype=out.dtype)
+    return g.lib().gqa_decode_attn_static_workspace(
+        ctypes.byref(desc), inp.q.data_ptr(), inp.k_cache.data_ptr(), inp.v_cache.data_ptr(),
+        inp.seqlens.data_ptr(), out.data_ptr(), lse.data_ptr(), splits,
+        torch.cuda.current_stream().cuda_stream)
+
+
+def _with_caller_workspace(inp, splits, causal, out_dtype):
+    out, lse = g.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, num_splits=splits, causal=causal,
+                        out_dtype=out_dtype)
+    return out, lse
+
+
+def test_static_workspace_matches_caller_workspace_on_consecutive_calls():
+    cases = [("llama8b", 0), ("spec", 0), ("llama70b", 8), ("llama8b", 0)]
+    for name, splits in cases:   # consecutive calls share the static array
+        cfg = workloads.CONFIGS[name]
+        inp = workloads.make_inputs(cfg).to(DEV)
+        need = g.gqa_decode_workspace_size(inp.q, inp.k_cache, splits, causal=cfg.causal)
+        assert 0 < need <= STATIC_BYTES
+        ref_out, ref_lse = _with_caller_workspace(inp, splits, cfg.causal, torch.bfloat16)
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        assert _static_call(inp, out, lse, splits, cfg.causal) == g.GQA_OK
+        torch.cuda.synchronize()
+        assert g.gqa_decode_get_error(clear=True) == g.GQA_OK
+        d_out = (out.double() - ref_out.double()).abs().max().item()
+        d_lse = (lse.double() - ref_lse.double()).abs().max().item()
+        assert d_out <= OUT_TOL and d_lse <= LSE_TOL, (name, d_out, d_lse)
+
+
+def test_static_workspace_refuses_problems_larger_than_it():
+    # 64 splits x 1024 rows x 128 floats alone fill the 32 MiB array
+    B, Hq, Hkv, d, s_max = 16, 64, 8, 128, 128
+    q = torch.randn(B, 1, Hq, d, device=DEV).to(torch.bfloat16)
+    k = torch.randn(B, s_max, Hkv, d, device=DEV).to(torch.bfloat16)
+    sl = torch.full((B,), s_max, dtype=torch.int32, device=DEV)
+    inp = workloads.DecodeInputs(None, q, k, k, sl, 0.0)
+    assert g.gqa_decode_workspace_size(q, k, 64) > STATIC_BYTES
+    out = torch.full((B, 1, Hq, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, 1, Hq), float("nan"), device=DEV)
+    assert _static_call(inp, out, lse, 64, False) == g.GQA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all() and torch.isnan(lse).all()   # nothing was launched
+    # the same problem with fewer splits fits and runs
+    assert _static_call(inp, out, lse, 8, False) == g.GQA_OK
+    torch.cuda.synchronize()
+    ref_out, ref_lse = _with_caller_workspace(inp, 8, False, torch.bfloat16)
+    assert (out.double() - ref_out.double()).abs().max().item() <= OUT_TOL
+    assert (lse.double() - ref_lse.double()).abs().max().item() <= LSE_TOL
