@@ -60,6 +60,30 @@ enum : unsigned { kErrTimeout = 1u, kErrBadSeqlen = 2u };
 // read and cleared by the host through gqa_decode_get_error().
 __device__ unsigned int g_gqa_error_bits = 0;
 
+// Optional per-CTA event trace (compile with -DGQA_TRACE): clock64 stamps of
+// each role's per-block steps, written to a buffer the host attaches with
+// gqa_trace_attach().  Compiled out otherwise.
+enum TraceEvent : int {
+  TR_START = 0, TR_SETUP = 1,
+  TR_PROD_WAIT = 2, TR_PROD_K = 3, TR_PROD_V = 4,
+  TR_MMA_K = 8, TR_MMA_QK = 9, TR_MMA_P = 10, TR_MMA_V = 11, TR_MMA_PV = 12,
+  TR_SM_S = 16, TR_SM_LD = 17, TR_SM_X = 18, TR_SM_PE = 19, TR_SM_PF = 20, TR_SM_E0 = 21, TR_SM_E1 = 22,
+  TR_END = 31, TR_EVENTS = 32
+};
+constexpr int kTraceBlocks = 64;
+#ifdef GQA_TRACE
+__device__ unsigned long long* g_gqa_trace_buf = nullptr;  // [grid][TR_EVENTS][kTraceBlocks]
+__device__ __forceinline__ void trace_event(int ev, uint32_t idx) {
+  unsigned long long* buf = g_gqa_trace_buf;
+  if (buf == nullptr) return;
+  const uint32_t i = idx < static_cast<uint32_t>(kTraceBlocks) ? idx : kTraceBlocks - 1;
+  buf[(static_cast<size_t>(blockIdx.x) * TR_EVENTS + ev) * kTraceBlocks + i] = clock64();
+}
+#define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event((ev), (idx))
+#else
+#define GQA_TRACE_EVENT(ev, idx) ((void)0)
+#endif
+
 constexpr int kThreads = 192;
 constexpr int kMaxSmemB = 1024;      // sequences whose lengths are staged in shared memory
 constexpr float kRescaleThreshold = 8.0f;
@@ -230,6 +254,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   // Inputs may be produced by the previous kernel in the stream.
   ptx::griddep_wait();
+  if (threadIdx.x == 0) GQA_TRACE_EVENT(TR_START, 0);
 
   if (lens_in_smem) {
     // clamped lengths, and (balanced plan) exclusive prefix sums of block counts
@@ -277,6 +302,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) GQA_TRACE_EVENT(TR_SETUP, 0);
   const int32_t* lens_raw = lens_in_smem ? s_len : p.seqlens;
 
   // =============================================================== producer
@@ -288,8 +314,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       bool have_prev = false, ok = true;
       int pb = 0, ph = 0, pblk = 0;
       // last tile issued per ring stage, for the drain on abort
+      [[maybe_unused]] uint32_t gk = 0, gv = 0;  // K / V blocks issued (trace indices)
       auto load_tile = [&](const CUtensorMap* map, int b, int h, int blk) -> bool {
         const uint32_t stage = t % NS, phase = (t / NS) & 1u;
+        if (map == &p.tm_k) GQA_TRACE_EVENT(TR_PROD_WAIT, gk);
         if (!ptx::mbar_wait_bounded(BAR(RING_EMPTY + stage), phase ^ 1u, abort_flag, p.timeout_ns))
           return false;
         ptx::mbar_arrive_expect_tx(BAR(RING_FULL + stage), Cfg::kSlotBytes);
@@ -298,6 +326,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         for (int kc = 0; kc < KCH; ++kc)
           ptx::tma_load_4d_hint(ptx::smem_u32(dst + kc * 16384), map, BAR(RING_FULL + stage), kc * 64, h,
                                 blk * kBlockN, b, policy);
+        if (map == &p.tm_k) GQA_TRACE_EVENT(TR_PROD_K, gk++);
+        else GQA_TRACE_EVENT(TR_PROD_V, gv++);
         ++t;
         return true;
       };
@@ -350,10 +380,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       auto issue_pv = [&](uint32_t gg, bool first_of_item) -> bool {
         const uint32_t sl = gg & 1u;
         if (!ptx::mbar_wait_bounded(BAR(P_FULL + sl), (gg >> 1) & 1u, abort_flag, p.timeout_ns)) return false;
+        GQA_TRACE_EVENT(TR_MMA_P, gg);
         const uint32_t vt = t++;
         const uint32_t stage = vt % NS;
         if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (vt / NS) & 1u, abort_flag, p.timeout_ns))
           return false;
+        GQA_TRACE_EVENT(TR_MMA_V, gg);
         ptx::tc_fence_after();
         const uint32_t v_addr = ptx::smem_u32(ring + stage * Cfg::kSlotBytes);
         const uint32_t p_addr = ptx::smem_u32(pbuf + sl * Cfg::kPBytes);
@@ -374,6 +406,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
         ptx::mma_commit(BAR(P_EMPTY + sl));
         ptx::mma_commit(BAR(RING_EMPTY + stage));
+        GQA_TRACE_EVENT(TR_MMA_PV, gg);
         return true;
       };
       WorkIter iter;
@@ -394,6 +427,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           const uint32_t stage = kt % NS;
           ok = ok && ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (kt / NS) & 1u, abort_flag, p.timeout_ns);
           if (!ok) break;
+          GQA_TRACE_EVENT(TR_MMA_K, g);
           ptx::tc_fence_after();
           const uint32_t k_addr = ptx::smem_u32(ring + stage * Cfg::kSlotBytes);
           const uint32_t s_col = sl ? kSCol1 : kSCol0;
@@ -405,6 +439,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           }
           ptx::mma_commit(BAR(S_FULL + sl));
           ptx::mma_commit(BAR(RING_EMPTY + stage));
+          GQA_TRACE_EVENT(TR_MMA_QK, g);
           if (blk == it.blk_end - 1) ptx::mma_commit(BAR(Q_EMPTY + qb));
           if (have_prev) {
             ok = issue_pv(prev_g, prev_first);
@@ -499,6 +534,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (!local_abort)
           local_abort = !ptx::mbar_wait_bounded(BAR(S_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns);
         local_abort = __any_sync(0xffffffffu, local_abort);
+        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_S, g);
         ptx::tc_fence_after();
         if (!local_abort) {
           const uint32_t s_col = sl ? kSCol1 : kSCol0;
@@ -517,6 +553,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0 && !local_abort) ptx::mbar_arrive(BAR(S_EMPTY + sl));  // S slot free for QK(g+2)
+        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_LD, g);
 
         // ---- mask: position pos is visible to column n when pos < L and,
         // with the causal mask, n / G >= pos - (L - nq)  (bottom-right)
@@ -536,6 +573,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
         const uint32_t fl = exchange((__any_sync(0xffffffffu, need) ? 1u : 0u) | (local_abort ? 2u : 0u), false, 0.f);
         if (fl & 2u) { aborted = true; break; }
+        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_X, g);
 
         // ---- correction (only when some column's max moved past the threshold)
         if (fl & 1u) {
@@ -585,6 +623,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (!local_abort)
           local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns);
         local_abort = __any_sync(0xffffffffu, local_abort);
+        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_PE, g);
         if (!local_abort) {
           // P^T as the K-major B operand: row n, position r, 128-byte swizzle
           uint8_t* pb = pbuf + sl * Cfg::kPBytes + (r >> 6) * (NPAD * 128);
@@ -617,11 +656,13 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0 && !local_abort) ptx::mbar_arrive(BAR(P_FULL + sl));
+        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_PF, g);
       }
       if (aborted) break;
 
       // ---------------------------------------------------------- epilogue
       const uint32_t gl = g - 1;
+      if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_E0, gl);
       if (!local_abort)
         local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag, p.timeout_ns);
       local_abort = __any_sync(0xffffffffu, local_abort);
@@ -685,6 +726,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       }
     }
+    if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_E1, g);
     if (aborted || local_abort) detail::set_error(kErrTimeout, abort_flag);
     // results of this CTA are written: dependents may launch
     ptx::griddep_launch_dependents();
@@ -693,6 +735,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // ---------------------------------------------------------------- teardown
   ptx::tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) GQA_TRACE_EVENT(TR_END, 0);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);

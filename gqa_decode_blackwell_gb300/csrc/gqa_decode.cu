@@ -558,6 +558,15 @@ gqa_status_t gqa_decode_plan(const gqa_desc_t* desc, const int32_t* seqlens_host
   return GQA_OK;
 }
 
+#ifdef GQA_TRACE
+// Trace builds only: attaches a device buffer of grid x TR_EVENTS x
+// kTraceBlocks uint64 for the decode kernel's event stamps (NULL detaches).
+gqa_status_t gqa_trace_attach(void* device_buffer) {
+  unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
+  return cudaMemcpyToSymbol(g_gqa_trace_buf, &p, sizeof p) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+#endif
+
 gqa_status_t gqa_decode_selftest_timeout(unsigned int timeout_us, void* stream) {
   if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return GQA_ERR_INVALID_ARG;
   selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(1000ull * timeout_us);
