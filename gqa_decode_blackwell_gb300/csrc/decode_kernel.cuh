@@ -14,16 +14,20 @@
 // the group (the PackGQA row order of "Flash Attention 4 - warp-role
 // choreography and the edges", section "Edge 2 - GQA").
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warp 0      TMA producer: Q per item, then K/V tiles into an mbarrier ring
 //               in the order K0 K1 V0 K2 V1 ... (the page's split-local order),
 //               so the score MMA of block i+1 can run while block i's softmax
 //               is in flight;
-//   warp 1      MMA issuer (one thread): QK(i+1) into the other of two S slots
-//               before PV(i) (the S/P ping-pong of "Optimization diaries: S/P
-//               ping-pong for FlashAttention-4 decode"); owns the TMEM
-//               allocation;
-//   warps 2..5  softmax / correction / epilogue warpgroup: thread r owns TMEM
+//   warp 1      score-MMA issuer (one thread): QK(i+1) goes into the other of
+//               two S slots while block i is in the softmax (the S/P
+//               ping-pong of "Optimization diaries: S/P ping-pong for
+//               FlashAttention-4 decode"); owns the TMEM allocation;
+//   warp 2      value-MMA issuer (one thread), as the KQ / VP MMA warps of
+//               the CUTLASS kernel ("Building a Faster GQA Decode Kernel for
+//               Blackwell SM100", section "Starting with the simple
+//               pipeline");
+//   warps 3..6  softmax / correction / epilogue warpgroup: thread r owns TMEM
 //               lane r = KV position r of S^T and row r of O^T.  It releases
 //               the S slot as soon as the scores are in registers, masks,
 //               votes on whether any column's max moved by more than the
@@ -65,7 +69,7 @@ __device__ unsigned int g_gqa_error_bits = 0;
 // gqa_trace_attach().  Compiled out otherwise.
 enum TraceEvent : int {
   TR_START = 0, TR_SETUP = 1,
-  TR_PROD_WAIT = 2, TR_PROD_K = 3, TR_PROD_V = 4,
+  TR_PROD_WAIT = 2, TR_PROD_K = 3, TR_PROD_V = 4, TR_PROD_PLAN = 5, TR_PROD_Q = 6,
   TR_MMA_K = 8, TR_MMA_QK = 9, TR_MMA_P = 10, TR_MMA_V = 11, TR_MMA_PV = 12,
   TR_SM_S = 16, TR_SM_LD = 17, TR_SM_X = 18, TR_SM_PE = 19, TR_SM_PF = 20, TR_SM_E0 = 21, TR_SM_E1 = 22,
   TR_END = 31, TR_EVENTS = 32
@@ -84,7 +88,8 @@ __device__ __forceinline__ void trace_event(int ev, uint32_t idx) {
 #define GQA_TRACE_EVENT(ev, idx) ((void)0)
 #endif
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;       // producer, QK issuer, PV issuer, 4 softmax warps
+constexpr int kSoftmaxThread0 = 96;  // first thread of the softmax warpgroup
 constexpr int kMaxSmemB = 1024;      // sequences whose lengths are staged in shared memory
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kTmemCols = 128;
@@ -197,7 +202,6 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   int32_t* s_pre = s_len + kMaxSmemB;                                   // [kMaxSmemB + 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_pre + kMaxSmemB + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* scan_tmp = reinterpret_cast<int32_t*>(tmem_slot + 2);      // [6] warp totals
 
   // barrier indices
   const uint32_t bar_base = ptx::smem_u32(bar);
@@ -207,10 +211,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
             DRAIN = 2 * NS + 12;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = p.plan.batch;
+  const PlanParams plan = p.plan;  // by value: iterators read it from registers
+  const int B = plan.batch;
   const bool lens_in_smem = B <= kMaxSmemB;
 
   // ---------------------------------------------------------------- set-up
+  // The producer warp only needs the barriers and the work plan: it computes
+  // the plan itself right after the grid dependency, publishes it through
+  // PLAN_READY and starts streaming, while the other warps allocate TMEM and
+  // zero the padding of the MMA operand buffers.
+  const int PLAN_READY = DRAIN + 2;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       ptx::mbar_init(BAR(RING_FULL + i), 1);
@@ -225,23 +235,58 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ptx::mbar_init(BAR(P_EMPTY + i), 1);
     }
     ptx::mbar_init(BAR(DRAIN), 1);
+    ptx::mbar_init(BAR(DRAIN + 1), 1);
+    ptx::mbar_init(BAR(PLAN_READY), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&p.tm_q);
     ptx::prefetch_tensormap(&p.tm_k);
     ptx::prefetch_tensormap(&p.tm_v);
   }
-  if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
-  }
-  // Padding rows of Q (beyond nq*G) and both P buffers start at zero; TMA
-  // never writes them.
-  {
+  __syncthreads();  // barriers initialised
+
+  uint32_t tmem_base = 0;
+  if (warp == 0) {
+    // Inputs may be produced by the previous kernel in the stream.
+    ptx::griddep_wait();
+    if (lane == 0) GQA_TRACE_EVENT(TR_START, 0);
+    if (lens_in_smem) {
+      // clamped lengths and the exclusive prefix sums of their block counts
+      for (int i = lane; i < B; i += 32) {
+        const int raw = p.seqlens[i];
+        const int L = clamp_len(raw, plan.max_seqlen);
+        if (raw != L) detail::set_error(kErrBadSeqlen, nullptr);
+        s_len[i] = L;
+      }
+      __syncwarp();
+      int run = 0;
+      for (int base = 0; base < B; base += 32) {
+        const int i = base + lane;
+        const int nb = i < B ? num_blocks(s_len[i]) : 0;
+        int incl = nb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (i < B) s_pre[i] = run + incl - nb;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) s_pre[B] = run;
+      __threadfence_block();
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(BAR(PLAN_READY));
+  } else {
+    if (warp == 1) {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish();
+    }
+    // Padding rows of Q (beyond nq*G) and both P buffers start at zero; TMA
+    // never writes them.
     const int nv = p.nq * p.G;
-    for (int i = threadIdx.x; i < 2 * KCH * NPAD; i += kThreads) {
+    const int tid = threadIdx.x - 32;
+    for (int i = tid; i < 2 * KCH * NPAD; i += kThreads - 32) {
       const int row = i % NPAD;
       if (row < nv) continue;
       uint4* dst = reinterpret_cast<uint4*>(qbuf + (i / NPAD) * NPAD * 128 + row * 128);
@@ -249,64 +294,26 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
     }
     uint4* pz = reinterpret_cast<uint4*>(pbuf);
-    for (int i = threadIdx.x; i < 2 * Cfg::kPBytes / 16; i += kThreads) pz[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < 2 * Cfg::kPBytes / 16; i += kThreads - 32) pz[i] = make_uint4(0, 0, 0, 0);
+    ptx::fence_proxy_async_smem();
+    // Outputs and workspace may still be read by the previous kernel.
+    ptx::griddep_wait();
+    if (!ptx::mbar_wait_bounded(BAR(PLAN_READY), 0, abort_flag, p.timeout_ns))
+      detail::set_error(kErrTimeout, abort_flag);
+    ptx::tc_fence_before();
+    ptx::named_barrier_sync(2, kThreads - 32);
+    ptx::tc_fence_after();
+    tmem_base = *tmem_slot;
+    if (threadIdx.x == 32) GQA_TRACE_EVENT(TR_SETUP, 0);
   }
-
-  // Inputs may be produced by the previous kernel in the stream.
-  ptx::griddep_wait();
-  if (threadIdx.x == 0) GQA_TRACE_EVENT(TR_START, 0);
-
-  if (lens_in_smem) {
-    // clamped lengths, and (balanced plan) exclusive prefix sums of block counts
-    constexpr int kCh = (kMaxSmemB + kThreads - 1) / kThreads;
-    int nb[kCh];
-    int local = 0;
-    const int i0 = threadIdx.x * kCh;
-#pragma unroll
-    for (int j = 0; j < kCh; ++j) {
-      const int i = i0 + j;
-      nb[j] = 0;
-      if (i < B) {
-        const int raw = p.seqlens[i];
-        const int L = clamp_len(raw, p.plan.max_seqlen);
-        if (raw != L) detail::set_error(kErrBadSeqlen, nullptr);
-        s_len[i] = L;
-        nb[j] = num_blocks(L);
-        local += nb[j];
-      }
-    }
-    if (p.plan.mode == PLAN_BALANCED) {
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) scan_tmp[warp] = incl;
-      __syncthreads();
-      int base = 0;
-      for (int w = 0; w < warp; ++w) base += scan_tmp[w];
-      int run = base + incl - local;
-#pragma unroll
-      for (int j = 0; j < kCh; ++j) {
-        const int i = i0 + j;
-        if (i < B) s_pre[i] = run;
-        run += nb[j];
-      }
-      if (i0 < B && i0 + kCh >= B) s_pre[B] = run;
-      if (B == 0 && threadIdx.x == 0) s_pre[0] = 0;
-    }
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  if (threadIdx.x == 0) GQA_TRACE_EVENT(TR_SETUP, 0);
+  // Uniform for warps 1..6: written (on a failed plan wait) before barrier 2.
+  const bool plan_ok = (warp == 0) || (*abort_flag == 0);
   const int32_t* lens_raw = lens_in_smem ? s_len : p.seqlens;
 
   // =============================================================== producer
-  if (warp == 0) {
+  if (!plan_ok) {
+    // the plan never arrived: nothing was issued, go straight to teardown
+  } else if (warp == 0) {
     if (lane == 0) {
       const uint64_t policy = ptx::l2_policy_evict_first();
       uint32_t t = 0;   // tiles issued into the ring
@@ -332,10 +339,11 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         return true;
       };
       WorkIter iter;
-      iter.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+      iter.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
       WorkItem it;
       while (ok && iter.next(it)) {
         if (it.blk_begin >= it.blk_end) continue;
+        GQA_TRACE_EVENT(TR_PROD_PLAN, static_cast<uint32_t>(kq));
         const int qb = kq & 1;
         if (!ptx::mbar_wait_bounded(BAR(Q_EMPTY + qb), ((kq >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
           ok = false;
@@ -346,6 +354,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         for (int kc = 0; kc < KCH; ++kc)
           ptx::tma_load_4d(ptx::smem_u32(qbuf + qb * Cfg::kQBytes + kc * NPAD * 128), &p.tm_q,
                            BAR(Q_FULL + qb), kc * 64, it.h * p.G, 0, it.b);
+        GQA_TRACE_EVENT(TR_PROD_Q, static_cast<uint32_t>(kq));
         ++kq;
         for (int blk = it.blk_begin; blk < it.blk_end && ok; ++blk) {
           ok = load_tile(&p.tm_k, it.b, it.h, blk);
@@ -366,97 +375,115 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     __syncwarp();
   }
-  // ============================================================ MMA issuer
-  else if (warp == 1) {
+  // ======================================================= MMA issuers
+  // Two single-thread issuers: warp 1 the score MMAs (QK), warp 2 the value
+  // MMAs (PV).  One issuing thread alone spends ~60 cycles per tcgen05.mma
+  // at these shapes; splitting the two kinds lets their issue overlap.  Each
+  // tracks its own tiles of the shared ring (order K0 K1 V0 K2 V1 ...: K of
+  // block g is tile 2g-1 (g > 0), V of block g is tile 2g+2, the CTA's last V
+  // is tile 2G-1) and releases them with its own commits.
+  else if (warp == 1 || warp == 2) {
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, NPAD, 0, 0);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, Cfg::kOWidth, 1, 0);
-      uint32_t t = 0;  // tiles consumed
-      uint32_t g = 0;  // blocks
-      int kq = 0;
-      bool ok = true, have_prev = false;
-      uint32_t prev_g = 0;
-      bool prev_first = false;
-      auto issue_pv = [&](uint32_t gg, bool first_of_item) -> bool {
-        const uint32_t sl = gg & 1u;
-        if (!ptx::mbar_wait_bounded(BAR(P_FULL + sl), (gg >> 1) & 1u, abort_flag, p.timeout_ns)) return false;
-        GQA_TRACE_EVENT(TR_MMA_P, gg);
-        const uint32_t vt = t++;
-        const uint32_t stage = vt % NS;
-        if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (vt / NS) & 1u, abort_flag, p.timeout_ns))
-          return false;
-        GQA_TRACE_EVENT(TR_MMA_V, gg);
-        ptx::tc_fence_after();
-        const uint32_t v_addr = ptx::smem_u32(ring + stage * Cfg::kSlotBytes);
-        const uint32_t p_addr = ptx::smem_u32(pbuf + sl * Cfg::kPBytes);
-        if constexpr (HEAD_DIM == 128) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t a = ptx::smem_desc_sw128(v_addr + k * 2048, 16384, 1024);
-            const uint64_t bd = ptx::smem_desc_sw128(p_addr + (k >> 2) * (NPAD * 128) + (k & 3) * 32, 16, 1024);
-            ptx::mma_bf16_ss(tmem_base + kOCol, a, bd, idesc_pv, (k > 0 || !first_of_item) ? 1u : 0u);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = ptx::smem_desc_sw128(v_addr + k * 2048, 8192, 1024);
-            const uint64_t bd = ptx::smem_desc_sw128(p_addr + k * 32, 16, 1024);
-            ptx::mma_bf16_ss(tmem_base + kOCol, a, bd, idesc_pv, (k > 0 || !first_of_item) ? 1u : 0u);
-          }
-        }
-        ptx::mma_commit(BAR(P_EMPTY + sl));
-        ptx::mma_commit(BAR(RING_EMPTY + stage));
-        GQA_TRACE_EVENT(TR_MMA_PV, gg);
-        return true;
-      };
+      const bool is_qk = (warp == 1);
+      const uint64_t ring_desc = ptx::smem_desc_sw128(ptx::smem_u32(ring), 16, 1024);
+      const uint64_t q_desc = ptx::smem_desc_sw128(ptx::smem_u32(qbuf), 16, 1024);
+      const uint64_t v_desc = ptx::smem_desc_sw128(ptx::smem_u32(ring), HEAD_DIM == 128 ? 16384 : 8192, 1024);
+      const uint64_t p_desc = ptx::smem_desc_sw128(ptx::smem_u32(pbuf), 16, 1024);
+      constexpr uint32_t kSlot16 = Cfg::kSlotBytes >> 4;  // descriptor units (16 B)
+      bool ok = true;
+      uint32_t g = 0;  // blocks of this CTA
+      int kq = 0;      // non-empty items
       WorkIter iter;
-      iter.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+      iter.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
       WorkItem it;
-      while (ok && iter.next(it)) {
-        if (it.blk_begin >= it.blk_end) continue;
-        const int qb = kq & 1;
-        if (!ptx::mbar_wait_bounded(BAR(Q_FULL + qb), (kq >> 1) & 1, abort_flag, p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        const uint32_t q_addr = ptx::smem_u32(qbuf + qb * Cfg::kQBytes);
-        for (int blk = it.blk_begin; blk < it.blk_end; ++blk) {
-          const uint32_t sl = g & 1u;
-          ok = ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns);
-          const uint32_t kt = t++;
-          const uint32_t stage = kt % NS;
-          ok = ok && ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (kt / NS) & 1u, abort_flag, p.timeout_ns);
-          if (!ok) break;
-          GQA_TRACE_EVENT(TR_MMA_K, g);
-          ptx::tc_fence_after();
-          const uint32_t k_addr = ptx::smem_u32(ring + stage * Cfg::kSlotBytes);
-          const uint32_t s_col = sl ? kSCol1 : kSCol0;
-#pragma unroll
-          for (int k = 0; k < HEAD_DIM / 16; ++k) {
-            const uint64_t a = ptx::smem_desc_sw128(k_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-            const uint64_t bq = ptx::smem_desc_sw128(q_addr + (k >> 2) * (NPAD * 128) + (k & 3) * 32, 16, 1024);
-            ptx::mma_bf16_ss(tmem_base + s_col, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+      if (is_qk) {
+        constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, NPAD, 0, 0);
+        while (ok && iter.next(it)) {
+          if (it.blk_begin >= it.blk_end) continue;
+          const int qb = kq & 1;
+          if (!ptx::mbar_wait_bounded(BAR(Q_FULL + qb), (kq >> 1) & 1, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
           }
-          ptx::mma_commit(BAR(S_FULL + sl));
-          ptx::mma_commit(BAR(RING_EMPTY + stage));
-          GQA_TRACE_EVENT(TR_MMA_QK, g);
-          if (blk == it.blk_end - 1) ptx::mma_commit(BAR(Q_EMPTY + qb));
-          if (have_prev) {
-            ok = issue_pv(prev_g, prev_first);
+          const uint64_t qd = q_desc + static_cast<uint64_t>(qb * (Cfg::kQBytes >> 4));
+          for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
+            const uint32_t sl = g & 1u;
+            const uint32_t kt = g == 0 ? 0u : 2u * g - 1u;
+            const uint32_t stage = kt % NS;
+            ok = ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns) &&
+                 ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (kt / NS) & 1u, abort_flag, p.timeout_ns);
             if (!ok) break;
+            GQA_TRACE_EVENT(TR_MMA_K, g);
+            ptx::tc_fence_after();
+            const uint64_t kd = ring_desc + static_cast<uint64_t>(stage * kSlot16);
+            const uint32_t d_tmem = tmem_base + (sl ? kSCol1 : kSCol0);
+#pragma unroll
+            for (int k = 0; k < HEAD_DIM / 16; ++k) {
+              const uint32_t off_a = static_cast<uint32_t>((k >> 2) * (16384 >> 4) + (k & 3) * 2);
+              const uint32_t off_b = static_cast<uint32_t>((k >> 2) * (NPAD * 128 >> 4) + (k & 3) * 2);
+              ptx::mma_bf16_ss(d_tmem, kd + off_a, qd + off_b, idesc_qk, k > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(BAR(S_FULL + sl));
+            ptx::mma_commit(BAR(RING_EMPTY + stage));
+            if (blk == it.blk_end - 1) ptx::mma_commit(BAR(Q_EMPTY + qb));
+            GQA_TRACE_EVENT(TR_MMA_QK, g);
           }
-          prev_g = g;
-          prev_first = (blk == it.blk_begin);
-          have_prev = true;
-          ++g;
+          ++kq;
         }
-        ++kq;
+      } else {
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, Cfg::kOWidth, 1, 0);
+        // total blocks of this CTA (to find its last V tile)
+        uint32_t g_total = 0;
+        {
+          WorkIter it0;
+          it0.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
+          WorkItem w0;
+          while (it0.next(w0)) g_total += static_cast<uint32_t>(w0.blk_end - w0.blk_begin);
+        }
+        while (ok && iter.next(it)) {
+          for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
+            const uint32_t sl = g & 1u;
+            const uint32_t vt = (g + 1 < g_total) ? 2u * g + 2u : 2u * g + 1u;
+            const uint32_t stage = vt % NS;
+            if (!ptx::mbar_wait_bounded(BAR(P_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            GQA_TRACE_EVENT(TR_MMA_P, g);
+            if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (vt / NS) & 1u, abort_flag, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            GQA_TRACE_EVENT(TR_MMA_V, g);
+            ptx::tc_fence_after();
+            const uint64_t vd = v_desc + static_cast<uint64_t>(stage * kSlot16);
+            const uint64_t pd = p_desc + static_cast<uint64_t>(sl * (Cfg::kPBytes >> 4));
+            const bool first = (blk == it.blk_begin);
+            if constexpr (HEAD_DIM == 128) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t off_b = static_cast<uint32_t>((k >> 2) * (NPAD * 128 >> 4) + (k & 3) * 2);
+                ptx::mma_bf16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)), pd + off_b,
+                                 idesc_pv, (k > 0 || !first) ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                ptx::mma_bf16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)),
+                                 pd + static_cast<uint32_t>(k * 2), idesc_pv, (k > 0 || !first) ? 1u : 0u);
+              }
+            }
+            ptx::mma_commit(BAR(P_EMPTY + sl));
+            ptx::mma_commit(BAR(RING_EMPTY + stage));
+            GQA_TRACE_EVENT(TR_MMA_PV, g);
+          }
+        }
       }
-      if (ok && have_prev) ok = issue_pv(prev_g, prev_first);
       if (!ok) detail::set_error(kErrTimeout, abort_flag);
-      // every MMA issued has completed before TMEM is released
-      ptx::mma_commit(BAR(DRAIN));
-      ptx::mbar_wait_bounded(BAR(DRAIN), 0, nullptr, p.timeout_ns);
+      // every MMA this thread issued has completed before TMEM is released
+      const uint32_t drain = BAR(DRAIN + (is_qk ? 0 : 1));
+      ptx::mma_commit(drain);
+      ptx::mbar_wait_bounded(drain, 0, nullptr, p.timeout_ns);
     }
     __syncwarp();
   }
@@ -466,7 +493,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int r = tq * 32 + lane;     // TMEM lane = KV row of S^T = row of O^T
     const uint32_t lane_addr = static_cast<uint32_t>(tq * 32) << 16;
     const int nv = p.nq * p.G;        // valid columns
-    const int rows_total = p.plan.batch * p.nq * p.Hq;
+    const int rows_total = plan.batch * p.nq * p.Hq;
     bool local_abort = false;
     uint32_t xc = 0;                  // exchange counter
 
@@ -490,20 +517,20 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     uint32_t g_total = 0;
     {
       WorkIter it0;
-      it0.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+      it0.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
       WorkItem w0;
       while (it0.next(w0)) g_total += static_cast<uint32_t>(w0.blk_end - w0.blk_begin);
     }
 
     WorkIter iter;
-    iter.init(&p.plan, lens_raw, s_len, s_pre, blockIdx.x);
+    iter.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
     WorkItem it;
     uint32_t g = 0;
     bool aborted = false;
     while (!aborted && iter.next(it)) {
       const int b = it.b, h = it.h;
-      const long long pair = static_cast<long long>(b) * p.plan.kv_heads + h;
-      if (it.first_piece && p.n_pieces != nullptr && threadIdx.x == 64) p.n_pieces[pair] = it.n_pieces;
+      const long long pair = static_cast<long long>(b) * plan.kv_heads + h;
+      if (it.first_piece && p.n_pieces != nullptr && threadIdx.x == kSoftmaxThread0) p.n_pieces[pair] = it.n_pieces;
       if (it.blk_begin >= it.blk_end) {
         // empty item: final output O = 0, lse = -inf; partial lse = -inf
         for (int n = 0; n < nv; ++n) {
@@ -534,7 +561,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (!local_abort)
           local_abort = !ptx::mbar_wait_bounded(BAR(S_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns);
         local_abort = __any_sync(0xffffffffu, local_abort);
-        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_S, g);
+        if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_S, g);
         ptx::tc_fence_after();
         if (!local_abort) {
           const uint32_t s_col = sl ? kSCol1 : kSCol0;
@@ -553,7 +580,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0 && !local_abort) ptx::mbar_arrive(BAR(S_EMPTY + sl));  // S slot free for QK(g+2)
-        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_LD, g);
+        if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_LD, g);
 
         // ---- mask: position pos is visible to column n when pos < L and,
         // with the causal mask, n / G >= pos - (L - nq)  (bottom-right)
@@ -573,7 +600,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
         const uint32_t fl = exchange((__any_sync(0xffffffffu, need) ? 1u : 0u) | (local_abort ? 2u : 0u), false, 0.f);
         if (fl & 2u) { aborted = true; break; }
-        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_X, g);
+        if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_X, g);
 
         // ---- correction (only when some column's max moved past the threshold)
         if (fl & 1u) {
@@ -623,7 +650,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (!local_abort)
           local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns);
         local_abort = __any_sync(0xffffffffu, local_abort);
-        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_PE, g);
+        if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_PE, g);
         if (!local_abort) {
           // P^T as the K-major B operand: row n, position r, 128-byte swizzle
           uint8_t* pb = pbuf + sl * Cfg::kPBytes + (r >> 6) * (NPAD * 128);
@@ -636,7 +663,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           // Tail block: V rows past the sequence end hold whatever the cache
           // holds there; zero them so that 0 * garbage cannot poison O.
           const int tail_rows = L - blk * kBlockN;
-          const int cap_rows = p.plan.max_seqlen - blk * kBlockN;
+          const int cap_rows = plan.max_seqlen - blk * kBlockN;
           if (tail_rows < kBlockN && cap_rows > tail_rows) {
             const uint32_t vt = (g + 1 < g_total) ? 2u * g + 2u : 2u * g + 1u;
             const uint32_t stage = vt % NS;
@@ -656,13 +683,13 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0 && !local_abort) ptx::mbar_arrive(BAR(P_FULL + sl));
-        if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_PF, g);
+        if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_PF, g);
       }
       if (aborted) break;
 
       // ---------------------------------------------------------- epilogue
       const uint32_t gl = g - 1;
-      if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_E0, gl);
+      if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_E0, gl);
       if (!local_abort)
         local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag, p.timeout_ns);
       local_abort = __any_sync(0xffffffffu, local_abort);
@@ -726,7 +753,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       }
     }
-    if (threadIdx.x == 64) GQA_TRACE_EVENT(TR_SM_E1, g);
+    if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_E1, g);
     if (aborted || local_abort) detail::set_error(kErrTimeout, abort_flag);
     // results of this CTA are written: dependents may launch
     ptx::griddep_launch_dependents();

@@ -542,7 +542,7 @@ gqa_status_t gqa_decode_plan(const gqa_desc_t* desc, const int32_t* seqlens_host
   if (desc->batch > 0) {
     for (int c = 0; c < hp.pp.num_ctas; ++c) {
       WorkIter it;
-      it.init(&hp.pp, seqlens_host, clamped.data(), pre.data(), c);
+      it.init(hp.pp, seqlens_host, clamped.data(), pre.data(), c);
       WorkItem w;
       while (it.next(w)) {
         if (items != nullptr && n < max_items) {

@@ -65,44 +65,58 @@ struct WorkItem {
 GQA_HD int clamp_len(int L, int s_max) { return L < 0 ? 0 : (L > s_max ? s_max : L); }
 GQA_HD int num_blocks(int L) { return (L + kBlockN - 1) / kBlockN; }
 
+// floor(a * b / c) for a, b >= 0 and c > 0.  GPUs emulate 64-bit division in
+// software, so the common case where everything fits in 32 bits takes the
+// 32-bit path.
+GQA_HD long long muldiv(long long a, long long b, long long c) {
+  const unsigned long long ab = static_cast<unsigned long long>(a) * static_cast<unsigned long long>(b);
+  if (ab <= 0xffffffffull && c <= 0xffffffffll)
+    return static_cast<long long>(static_cast<uint32_t>(ab) / static_cast<uint32_t>(c));
+  return static_cast<long long>(ab / static_cast<unsigned long long>(c));
+}
+
+// floor(a / c) for a >= 0, c > 0, with the same 32-bit fast path.
+GQA_HD long long div_nonneg(long long a, long long c) { return muldiv(a, 1, c); }
+
 // CTA owning unit u under the balanced partition of U units over C CTAs:
 // the largest c with floor(c*U/C) <= u.
 GQA_HD int balanced_cta_of(long long u, long long U, int C) {
-  return static_cast<int>(((u + 1) * static_cast<long long>(C) - 1) / U);
+  return static_cast<int>(div_nonneg((u + 1) * static_cast<long long>(C) - 1, U));
 }
 
 // Round-robin over split items.  `lens` holds raw lengths (clamped here).
 struct SplitIter {
-  const PlanParams* pp;
+  PlanParams pp;
   const int32_t* lens;
   long long w, total;
   int cta;
 
-  GQA_HD void init(const PlanParams* p, const int32_t* l, int c) {
+  GQA_HD void init(const PlanParams& p, const int32_t* l, int c) {
     pp = p; lens = l; cta = c; w = c;
-    total = static_cast<long long>(p->batch) * p->kv_heads * p->num_splits;
+    total = static_cast<long long>(p.batch) * p.kv_heads * p.num_splits;
   }
   GQA_HD bool next(WorkItem& it) {
     if (w >= total) return false;
-    const int S = pp->num_splits;
-    const int s = static_cast<int>(w % S);
-    const long long pair = w / S;
-    it.h = static_cast<int>(pair % pp->kv_heads);
-    it.b = static_cast<int>(pair / pp->kv_heads);
-    it.L = clamp_len(lens[it.b], pp->max_seqlen);
+    const int S = pp.num_splits;
+    const long long pair = div_nonneg(w, S);
+    const int s = static_cast<int>(w - pair * S);
+    const long long bb = div_nonneg(pair, pp.kv_heads);
+    it.h = static_cast<int>(pair - bb * pp.kv_heads);
+    it.b = static_cast<int>(bb);
+    it.L = clamp_len(lens[it.b], pp.max_seqlen);
     const int nblk = num_blocks(it.L);
-    int splits = (nblk + pp->min_blocks - 1) / pp->min_blocks;
+    int splits = (nblk + pp.min_blocks - 1) / pp.min_blocks;
     splits = splits < 1 ? 1 : (splits > S ? S : splits);
     if (s < splits) {
-      it.blk_begin = static_cast<int>(static_cast<long long>(s) * nblk / splits);
-      it.blk_end = static_cast<int>(static_cast<long long>(s + 1) * nblk / splits);
+      it.blk_begin = static_cast<int>(muldiv(s, nblk, splits));
+      it.blk_end = static_cast<int>(muldiv(s + 1, nblk, splits));
     } else {
       it.blk_begin = it.blk_end = 0;
     }
-    it.slot = (S == 1 && !pp->force_partial) ? -1 : s;
+    it.slot = (S == 1 && !pp.force_partial) ? -1 : s;
     it.first_piece = (s == 0);
     it.n_pieces = splits;
-    w += pp->num_ctas;
+    w += pp.num_ctas;
     return true;
   }
 };
@@ -110,23 +124,23 @@ struct SplitIter {
 // Contiguous equal ranges of units.  `lens` are clamped lengths and `pre` the
 // exclusive prefix sums of their block counts (B + 1 entries).
 struct BalancedIter {
-  const PlanParams* pp;
   const int32_t* lens;
   const int32_t* pre;
   long long U, lo, hi;
+  int B, H;
   int b, h, cta, C;  // C: effective CTA count min(num_ctas, U), at least 1
 
-  GQA_HD void init(const PlanParams* p, const int32_t* l, const int32_t* prefix, int c) {
-    pp = p; lens = l; pre = prefix; cta = c;
-    const int B = p->batch, H = p->kv_heads;
+  GQA_HD void init(const PlanParams& p, const int32_t* l, const int32_t* prefix, int c) {
+    lens = l; pre = prefix; cta = c;
+    B = p.batch; H = p.kv_heads;
     U = static_cast<long long>(H) * pre[B];
-    C = U <= 0 ? 1 : (U < p->num_ctas ? static_cast<int>(U) : p->num_ctas);
+    C = U <= 0 ? 1 : (U < p.num_ctas ? static_cast<int>(U) : p.num_ctas);
     if (c >= C) {  // this CTA owns nothing
       b = B; h = 0; lo = hi = U;
       return;
     }
-    lo = static_cast<long long>(c) * U / C;
-    hi = static_cast<long long>(c + 1) * U / C;
+    lo = muldiv(c, U, C);
+    hi = muldiv(c + 1, U, C);
     // first pair: smallest b whose units end after lo, or that starts at or after lo
     int a = 0, z = B;
     while (a < z) {
@@ -140,14 +154,13 @@ struct BalancedIter {
     if (b < B) {
       const long long start = static_cast<long long>(H) * pre[b];
       const int nblk = pre[b + 1] - pre[b];
-      if (start < lo && nblk > 0) h = static_cast<int>((lo - start) / nblk);
+      if (start < lo && nblk > 0) h = static_cast<int>(div_nonneg(lo - start, nblk));
     }
   }
   GQA_HD void advance() {
-    if (++h == pp->kv_heads) { h = 0; ++b; }
+    if (++h == H) { h = 0; ++b; }
   }
   GQA_HD bool next(WorkItem& it) {
-    const int B = pp->batch, H = pp->kv_heads;
     while (b < B) {
       const int nblk = pre[b + 1] - pre[b];
       const long long u_first = static_cast<long long>(H) * pre[b] + static_cast<long long>(h) * nblk;
@@ -189,9 +202,9 @@ struct WorkIter {
   SplitIter s;
   BalancedIter bal;
   int mode;
-  GQA_HD void init(const PlanParams* p, const int32_t* raw_lens, const int32_t* clamped_lens,
+  GQA_HD void init(const PlanParams& p, const int32_t* raw_lens, const int32_t* clamped_lens,
                    const int32_t* prefix, int cta) {
-    mode = p->mode;
+    mode = p.mode;
     if (mode == PLAN_BALANCED) bal.init(p, clamped_lens, prefix, cta);
     else s.init(p, raw_lens, cta);
   }
