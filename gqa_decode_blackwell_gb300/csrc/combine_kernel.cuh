@@ -5,8 +5,8 @@
 // Partials are normalised (O_s, lse_s) in fp32.  For one output row:
 //   M = max_s lse_s;  w_s = exp(lse_s - M);  O = sum_s w_s O_s / sum_s w_s;
 //   lse = M + ln(sum_s w_s).
-// A split with lse_s = -inf is empty and is never read; a row whose splits are
-// all empty gets O = 0 and lse = -inf.  The splits are summed in a fixed order,
+// A split with lse_s = -inf is empty and its partial is ignored; a row whose
+// splits are all empty gets O = 0 and lse = -inf.  The splits are summed in a fixed order,
 // so the output is bit-identical from run to run, and the maximum is taken here
 // from the staged lse values (no global running-max buffer, nothing to reset).
 //
@@ -26,7 +26,7 @@ constexpr int kMaxSplits = 64;
 struct CombineParams {
   const float* o_part;      // [num_slots, rows, d]
   const float* lse_part;    // [num_slots, rows]
-  const int32_t* n_pieces;  // optional [B * Hkv]: valid slots per pair (balanced plan)
+  const int32_t* n_pieces;  // optional [B * Hkv][4]: valid slots per pair in [0] (balanced plan)
   void* out;                // [rows, d] bf16 or fp32
   float* lse;               // [rows] or null
   long long rows;
@@ -46,17 +46,46 @@ gqa_combine_kernel(const CombineParams p) {
   const long long row = static_cast<long long>(blockIdx.x) * (kCombineThreads / 32) + (threadIdx.x >> 5);
   if (row >= p.rows) return;
 
-  int n = p.num_splits;
+  // Every load below is independent of the others, so they are all issued
+  // before the first use: the piece count, the LSEs of every allocated slot
+  // and the first kSpec partial rows.  Slots beyond the valid count are
+  // allocated memory whose values are masked out, never used.
+  constexpr int kSpec = 4;
+  const int slots = p.num_splits;  // allocated slots
+  int n = slots;
+  const int* np_ptr = nullptr;
   if (p.n_pieces != nullptr) {
     const long long bt = row / p.Hq;            // b * nq + t
     const int hq = static_cast<int>(row % p.Hq);
     const long long b = bt / p.nq;
-    n = p.n_pieces[b * p.kv_heads + hq / p.G];
+    np_ptr = p.n_pieces + (b * p.kv_heads + hq / p.G) * 4;  // one 16-byte record per pair
+  }
+  const int n_raw = np_ptr != nullptr ? *np_ptr : slots;
+  float l0 = lane < slots ? p.lse_part[static_cast<long long>(lane) * p.rows + row] : -INFINITY;
+  float l1 = lane + 32 < slots ? p.lse_part[static_cast<long long>(lane + 32) * p.rows + row] : -INFINITY;
+  float spec[kSpec][VEC];
+#pragma unroll
+  for (int s = 0; s < kSpec; ++s) {
+    if (s < slots) {
+      const float* src = p.o_part + (static_cast<long long>(s) * p.rows + row) * HEAD_DIM + lane * VEC;
+      if constexpr (VEC == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+        spec[s][0] = v.x; spec[s][1] = v.y; spec[s][2] = v.z; spec[s][3] = v.w;
+      } else {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+        spec[s][0] = v.x; spec[s][1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) spec[s][i] = 0.f;
+    }
+  }
+  if (np_ptr != nullptr) {
+    n = n_raw < slots ? n_raw : slots;
     if (n <= 1) return;                          // written directly by the decode kernel
   }
-
-  const float l0 = lane < n ? p.lse_part[static_cast<long long>(lane) * p.rows + row] : -INFINITY;
-  const float l1 = lane + 32 < n ? p.lse_part[static_cast<long long>(lane + 32) * p.rows + row] : -INFINITY;
+  if (lane >= n) l0 = -INFINITY;
+  if (lane + 32 >= n) l1 = -INFINITY;
   float M = fmaxf(l0, l1);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -73,9 +102,17 @@ gqa_combine_kernel(const CombineParams p) {
     float W = w0 + w1;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-    for (int s = 0; s < n; ++s) {
+#pragma unroll
+    for (int s = 0; s < kSpec; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w0, s);
+      if (s < n && ws != 0.f) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] += ws * spec[s][i];
+      }
+    }
+    for (int s = kSpec; s < n; ++s) {
       const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      if (ws == 0.f) continue;  // empty split (or a weight that underflows): not read
+      if (ws == 0.f) continue;  // empty split (or a weight that underflows): not used
       const float* src = p.o_part + (static_cast<long long>(s) * p.rows + row) * HEAD_DIM + lane * VEC;
       if constexpr (VEC == 4) {
         const float4 v = __ldg(reinterpret_cast<const float4*>(src));

@@ -77,14 +77,17 @@ enum TraceEvent : int {
 constexpr int kTraceBlocks = 64;
 #ifdef GQA_TRACE
 __device__ unsigned long long* g_gqa_trace_buf = nullptr;  // [grid][TR_EVENTS][kTraceBlocks]
-__device__ __forceinline__ void trace_event(int ev, uint32_t idx) {
-  unsigned long long* buf = g_gqa_trace_buf;
+__device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uint32_t idx) {
   if (buf == nullptr) return;
   const uint32_t i = idx < static_cast<uint32_t>(kTraceBlocks) ? idx : kTraceBlocks - 1;
   buf[(static_cast<size_t>(blockIdx.x) * TR_EVENTS + ev) * kTraceBlocks + i] = clock64();
 }
-#define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event((ev), (idx))
+// The buffer address is read once per thread (GQA_TRACE_SETUP) so that an
+// event costs a clock read and a store, not a dependent global load.
+#define GQA_TRACE_SETUP() unsigned long long* const gqa_trace_buf_ = ::gqa::g_gqa_trace_buf
+#define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event(gqa_trace_buf_, (ev), (idx))
 #else
+#define GQA_TRACE_SETUP() ((void)0)
 #define GQA_TRACE_EVENT(ev, idx) ((void)0)
 #endif
 
@@ -110,6 +113,7 @@ struct DecodeParams {
   int out_fp32;
   int causal;
   float scale_log2;   // softmax scale * log2(e)
+  int lse_bulk;       // LSE rows may be written by 16-byte bulk copies (G % 4 == 0, aligned)
   unsigned long long timeout_ns;
 };
 
@@ -122,8 +126,10 @@ struct DecodeCfg {
   static constexpr int kOWidth = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // TMEM columns of O
   // fixed part of shared memory after the ring
   static constexpr int kXchgBytes = 2 * (4 * 4 + 4 * NPAD * 4);
-  static constexpr int kMiscBytes = 512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64;
-  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes;
+  static constexpr int kMiscBytes = (512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64 + 127) / 128 * 128;
+  // output staging: one item's rows (fp32 worst case), its LSEs, its piece count
+  static constexpr int kOutBytes = NPAD * HEAD_DIM * 4 + 128 + 16;
+  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes + kOutBytes;
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // minus alignment slack
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kSlotBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
@@ -132,6 +138,7 @@ struct DecodeCfg {
   static_assert(kStages >= 4, "ring too shallow");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory over budget");
   static_assert(kOWidth <= 64 && NPAD <= 32, "TMEM column plan");
+  static_assert(kMiscBytes % 128 == 0 && (2 * kQBytes + 2 * kPBytes) % 128 == 0, "staging alignment");
 };
 
 namespace detail {
@@ -188,6 +195,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HEAD_DIM, NPAD>;
   constexpr int NS = Cfg::kStages;
   constexpr int KCH = Cfg::kChunks;
+  GQA_TRACE_SETUP();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -202,6 +210,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   int32_t* s_pre = s_len + kMaxSmemB;                                   // [kMaxSmemB + 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_pre + kMaxSmemB + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* obuf = misc + Cfg::kMiscBytes;                                 // output rows
+  float* lse_stage = reinterpret_cast<float*>(obuf + NPAD * HEAD_DIM * 4);  // [32]
+  int32_t* np_stage = reinterpret_cast<int32_t*>(lse_stage + 32);         // [4]
 
   // barrier indices
   const uint32_t bar_base = ptx::smem_u32(bar);
@@ -511,7 +522,27 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ptx::named_barrier_sync(1, 128);
       return xflags[buf * 4 + 0] | xflags[buf * 4 + 1] | xflags[buf * 4 + 2] | xflags[buf * 4 + 3];
     };
-    auto xval = [&](int w, int col) -> float { return xvals[(((xc - 1) & 1u) * 4 + w) * NPAD + col]; };
+    // Per-column combination of the four warps' values of the last exchange,
+    // read as 16-byte vectors.
+    auto xcombine = [&](float (&outv)[NPAD], bool is_max) {
+      const float4* base = reinterpret_cast<const float4*>(xvals + ((xc - 1) & 1u) * 4 * NPAD);
+#pragma unroll
+      for (int c4 = 0; c4 < NPAD / 4; ++c4) {
+        const float4 a = base[0 * (NPAD / 4) + c4], b4 = base[1 * (NPAD / 4) + c4];
+        const float4 c = base[2 * (NPAD / 4) + c4], d4 = base[3 * (NPAD / 4) + c4];
+        if (is_max) {
+          outv[4 * c4 + 0] = fmaxf(fmaxf(a.x, b4.x), fmaxf(c.x, d4.x));
+          outv[4 * c4 + 1] = fmaxf(fmaxf(a.y, b4.y), fmaxf(c.y, d4.y));
+          outv[4 * c4 + 2] = fmaxf(fmaxf(a.z, b4.z), fmaxf(c.z, d4.z));
+          outv[4 * c4 + 3] = fmaxf(fmaxf(a.w, b4.w), fmaxf(c.w, d4.w));
+        } else {
+          outv[4 * c4 + 0] = (a.x + b4.x) + (c.x + d4.x);
+          outv[4 * c4 + 1] = (a.y + b4.y) + (c.y + d4.y);
+          outv[4 * c4 + 2] = (a.z + b4.z) + (c.z + d4.z);
+          outv[4 * c4 + 3] = (a.w + b4.w) + (c.w + d4.w);
+        }
+      }
+    };
 
     // total blocks of this CTA (to locate the last V tile in the ring)
     uint32_t g_total = 0;
@@ -522,6 +553,45 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       while (it0.next(w0)) g_total += static_cast<uint32_t>(w0.blk_end - w0.blk_begin);
     }
 
+    // Makes the staged rows of one item visible to the async proxy and has one
+    // thread write them with bulk copies: nq copies of G contiguous rows (the
+    // G query heads of one token) for O, the same for the LSEs, and (balanced
+    // plan) the pair's piece count.  A plain global store could wait behind
+    // the in-flight TMA loads of this SM for microseconds and hold the whole
+    // warpgroup; the bulk copies are asynchronous.
+    auto issue_outputs = [&](const WorkItem& wi, long long pair_idx, bool with_o) {
+      ptx::fence_proxy_async_smem();
+      ptx::named_barrier_sync(1, 128);
+      if (threadIdx.x != kSoftmaxThread0) return;
+      const bool final_out = wi.slot < 0;
+      const uint32_t esz = (final_out && !p.out_fp32) ? 2u : 4u;
+      const uint32_t row_bytes = static_cast<uint32_t>(p.G) * HEAD_DIM * esz;
+      for (int t = 0; t < p.nq; ++t) {
+        const long long row0 = (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G;
+        if (final_out || with_o) {
+          uint8_t* dst = final_out
+              ? static_cast<uint8_t*>(p.out) + row0 * HEAD_DIM * esz
+              : reinterpret_cast<uint8_t*>(p.o_part + (static_cast<long long>(wi.slot) * rows_total + row0) * HEAD_DIM);
+          ptx::bulk_store(dst, ptx::smem_u32(obuf + static_cast<uint32_t>(t) * row_bytes), row_bytes);
+        }
+        float* lse_dst = final_out ? (p.lse != nullptr ? p.lse + row0 : nullptr)
+                                   : p.lse_part + static_cast<long long>(wi.slot) * rows_total + row0;
+        if (lse_dst != nullptr) {
+          if (p.lse_bulk) {
+            ptx::bulk_store(lse_dst, ptx::smem_u32(lse_stage + t * p.G), static_cast<uint32_t>(p.G) * 4u);
+          } else {
+            for (int g2 = 0; g2 < p.G; ++g2) lse_dst[g2] = lse_stage[t * p.G + g2];
+          }
+        }
+      }
+      if (wi.first_piece && p.n_pieces != nullptr) {
+        np_stage[0] = wi.n_pieces;
+        ptx::fence_proxy_async_smem();
+        ptx::bulk_store(p.n_pieces + pair_idx * 4, ptx::smem_u32(np_stage), 16u);
+      }
+      ptx::bulk_commit();
+    };
+
     WorkIter iter;
     iter.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
     WorkItem it;
@@ -530,22 +600,20 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     while (!aborted && iter.next(it)) {
       const int b = it.b, h = it.h;
       const long long pair = static_cast<long long>(b) * plan.kv_heads + h;
-      if (it.first_piece && p.n_pieces != nullptr && threadIdx.x == kSoftmaxThread0) p.n_pieces[pair] = it.n_pieces;
       if (it.blk_begin >= it.blk_end) {
         // empty item: final output O = 0, lse = -inf; partial lse = -inf
-        for (int n = 0; n < nv; ++n) {
-          const int t = n / p.G, hq = h * p.G + n % p.G;
-          const long long row = (static_cast<long long>(b) * p.nq + t) * p.Hq + hq;
-          if (it.slot < 0) {
-            if (r < HEAD_DIM) {
-              if (p.out_fp32) static_cast<float*>(p.out)[row * HEAD_DIM + r] = 0.f;
-              else static_cast<__nv_bfloat16*>(p.out)[row * HEAD_DIM + r] = __float2bfloat16_rn(0.f);
-            }
-            if (r == 0 && p.lse != nullptr) p.lse[row] = -INFINITY;
-          } else if (r == 0) {
-            p.lse_part[static_cast<long long>(it.slot) * rows_total + row] = -INFINITY;
+        if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_read_all();
+        ptx::named_barrier_sync(1, 128);  // staging free
+        if (r < HEAD_DIM) {
+          for (int n = 0; n < nv; ++n) {
+            if (it.slot < 0 && !p.out_fp32)
+              reinterpret_cast<__nv_bfloat16*>(obuf)[n * HEAD_DIM + r] = __float2bfloat16_rn(0.f);
+            else
+              reinterpret_cast<float*>(obuf)[n * HEAD_DIM + r] = 0.f;
           }
         }
+        if (r < nv) lse_stage[r] = -INFINITY;
+        issue_outputs(it, pair, false);
         continue;
       }
       const int L = it.L;
@@ -613,11 +681,11 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           local_abort = __any_sync(0xffffffffu, local_abort);
           const uint32_t f2 = exchange(local_abort ? 2u : 0u, true, wmax);
           if (f2 & 2u) { aborted = true; break; }
-          float alpha[NPAD];
+          float alpha[NPAD], bmax[NPAD];
+          xcombine(bmax, true);
 #pragma unroll
           for (int n = 0; n < NPAD; ++n) {
-            const float bm = fmaxf(fmaxf(xval(0, n), xval(1, n)), fmaxf(xval(2, n), xval(3, n)));
-            const float mn = fmaxf(m[n], bm);
+            const float mn = fmaxf(m[n], bmax[n]);
             const float ms = mn == -INFINITY ? 0.f : mn;
             alpha[n] = ptx::ex2_approx(m[n] - ms);
             m[n] = mn;
@@ -694,11 +762,11 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag, p.timeout_ns);
       local_abort = __any_sync(0xffffffffu, local_abort);
       const float lsum = detail::transpose_reduce<NPAD, false>(l, lane);
+      if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_read_all();  // staging free after f3
       const uint32_t f3 = exchange(local_abort ? 2u : 0u, true, lsum);
       if (f3 & 2u) { aborted = true; break; }
       float lt[NPAD];
-#pragma unroll
-      for (int n = 0; n < NPAD; ++n) lt[n] = (xval(0, n) + xval(1, n)) + (xval(2, n) + xval(3, n));
+      xcombine(lt, false);
 
       ptx::tc_fence_after();
       float o[Cfg::kOWidth];
@@ -716,44 +784,46 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       if constexpr (HEAD_DIM == 64) {
         // lanes 64..127 hold the second half-block's contribution in columns [N, 2N)
         float* xo = reinterpret_cast<float*>(pbuf);  // both P buffers are idle here
+        // [n][row] layout: the 32 lanes of a warp touch 32 consecutive words
         if (r >= 64) {
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) xo[(r - 64) * NPAD + n] = o[NPAD + n];
+          for (int n = 0; n < NPAD; ++n) xo[n * 64 + (r - 64)] = o[NPAD + n];
         }
         ptx::named_barrier_sync(1, 128);
         if (r < 64) {
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) o[n] += xo[r * NPAD + n];
+          for (int n = 0; n < NPAD; ++n) o[n] += xo[n * 64 + r];
         }
         ptx::named_barrier_sync(1, 128);  // xo is read before P is rewritten
         writer = r < 64;
       }
+      // Outputs go to shared memory in their global layout (row n = t*G + g
+      // of this pair, d contiguous) and leave by bulk copies (issue_outputs).
       if (writer) {
+        const bool as_bf16 = it.slot < 0 && !p.out_fp32;
 #pragma unroll
         for (int n = 0; n < NPAD; ++n) {
-          if (n >= nv) break;
-          const int t = n / p.G, hq = h * p.G + n % p.G;
-          const long long row = (static_cast<long long>(b) * p.nq + t) * p.Hq + hq;
-          const float inv = lt[n] > 0.f ? 1.0f / lt[n] : 0.f;
+          const float inv = lt[n] > 0.f ? ptx::rcp_approx(lt[n]) : 0.f;
           const float val = o[n] * inv;
-          if (it.slot < 0) {
-            if (p.out_fp32) static_cast<float*>(p.out)[row * HEAD_DIM + d_row] = val;
-            else static_cast<__nv_bfloat16*>(p.out)[row * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
-          } else {
-            p.o_part[(static_cast<long long>(it.slot) * rows_total + row) * HEAD_DIM + d_row] = val;
-          }
-          if (d_row == n) {
-            const float lse = lt[n] > 0.f ? 0.69314718055994531f * (m[n] + __log2f(lt[n])) : -INFINITY;
-            if (it.slot < 0) {
-              if (p.lse != nullptr) p.lse[row] = lse;
-            } else {
-              p.lse_part[static_cast<long long>(it.slot) * rows_total + row] = lse;
-            }
+          if (n < nv) {
+            if (as_bf16) reinterpret_cast<__nv_bfloat16*>(obuf)[n * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
+            else reinterpret_cast<float*>(obuf)[n * HEAD_DIM + d_row] = val;
           }
         }
+        if (d_row < nv) {
+          float lt_n = 0.f, m_n = 0.f;
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n)
+            if (n == d_row) { lt_n = lt[n]; m_n = m[n]; }
+          lse_stage[d_row] = lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
+        }
       }
+      issue_outputs(it, pair, true);
     }
-    if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_E1, g);
+    if (threadIdx.x == kSoftmaxThread0) {
+      ptx::bulk_wait_all();  // this CTA's outputs are in global memory
+      GQA_TRACE_EVENT(TR_SM_E1, g);
+    }
     if (aborted || local_abort) detail::set_error(kErrTimeout, abort_flag);
     // results of this CTA are written: dependents may launch
     ptx::griddep_launch_dependents();

@@ -174,7 +174,7 @@ WsLayout ws_layout(const gqa_desc_t* d, const HostPlan& hp) {
   w.o_off = 0;
   w.lse_off = round_up(slots * rows * d->head_dim * sizeof(float), kWsAlign);
   w.np_off = w.lse_off + round_up(slots * rows * sizeof(float), kWsAlign);
-  w.total = w.np_off + round_up(static_cast<size_t>(d->batch) * d->kv_heads * sizeof(int32_t), kWsAlign);
+  w.total = w.np_off + round_up(static_cast<size_t>(d->batch) * d->kv_heads * 4 * sizeof(int32_t), kWsAlign);
   return w;
 }
 
@@ -284,6 +284,7 @@ gqa_status_t prepare_decode(const gqa_desc_t* d, const void* q, const void* k, c
   p->causal = d->causal != 0;
   const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
   p->scale_log2 = scale * 1.4426950408889634f;
+  p->lse_bulk = (p->G % 4) == 0;  // LSE rows of G floats: 16-byte multiples
   p->timeout_ns = wait_timeout_ns();
   return GQA_OK;
 }
@@ -348,6 +349,7 @@ gqa_status_t attn_impl(const gqa_desc_t* desc, const void* q, const void* k_cach
     if ((rc = prepare_decode(desc, q, k_cache, v_cache, seqlens, hp, &p)) != GQA_OK) return rc;
     p.out = out;
     p.lse = lse;
+    if (lse != nullptr && !aligned(lse, 16)) p.lse_bulk = 0;
     p.o_part = o_part;
     p.lse_part = lse_part;
     p.n_pieces = n_pieces;

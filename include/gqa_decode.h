@@ -166,7 +166,7 @@ gqa_status_t gqa_decode_attn_merge(const gqa_desc_t* desc, void* out, float* lse
  *   o_part    fp32 [num_splits, B, nq, Hq, d], 16-byte aligned
  *   lse_part  fp32 [num_splits, B, nq, Hq]; lse_part = -inf marks an empty
  *             split (s >= splits_b, or no visible key), whose o_part entries
- *             are left unwritten
+ *             are left unwritten (gqa_decode_combine ignores them)
  * num_splits: 1..64.  gqa_decode_combine merges the result.
  */
 gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const void* k_cache,
@@ -178,8 +178,9 @@ gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const voi
  * for Blackwell SM100", section "Combining the KV splits"): per row,
  * M = max_s lse_s, w_s = exp(lse_s - M), O = sum_s w_s O_s / sum_s w_s,
  * lse = M + ln sum_s w_s, summing splits in index order (bit-reproducible).
- * Splits with lse_s = -inf are skipped and their o_part never read; a row
- * with no valid split gets O = 0, lse = -inf.
+ * Splits with lse_s = -inf are skipped (their o_part values are ignored and
+ * may be anything, NaN included); a row with no valid split gets O = 0,
+ * lse = -inf.
  *   o_part    fp32 [num_splits, rows, head_dim], 16-byte aligned
  *   lse_part  fp32 [num_splits, rows]
  *   out       [rows, head_dim] of out_dtype, 16-byte aligned
