@@ -93,7 +93,8 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 
 constexpr int kThreads = 224;       // producer, QK issuer, PV issuer, 4 softmax warps
 constexpr int kSoftmaxThread0 = 96;  // first thread of the softmax warpgroup
-constexpr int kMaxSmemB = 1024;      // sequences whose lengths are staged in shared memory
+constexpr int kMaxSmemB = 512;       // sequences whose lengths are staged in shared memory
+constexpr int kMaxListItems = 128;   // work items of one CTA kept as a list in shared memory
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kSCol0 = 0, kSCol1 = 32, kOCol = 64;
@@ -126,7 +127,9 @@ struct DecodeCfg {
   static constexpr int kOWidth = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // TMEM columns of O
   // fixed part of shared memory after the ring
   static constexpr int kXchgBytes = 2 * (4 * 4 + 4 * NPAD * 4);
-  static constexpr int kMiscBytes = (512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64 + 127) / 128 * 128;
+  static constexpr int kListBytes = 16 + kMaxListItems * static_cast<int>(sizeof(WorkItem));
+  static constexpr int kMiscBytes =
+      (512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64 + kListBytes + 127) / 128 * 128;
   // output staging: one item's rows (fp32 worst case), its LSEs, its piece count
   static constexpr int kOutBytes = NPAD * HEAD_DIM * 4 + 128 + 16;
   static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes + kOutBytes;
@@ -189,6 +192,29 @@ __device__ __forceinline__ void set_error(unsigned bits, volatile int* abort_fla
 
 }  // namespace detail
 
+// Work items of one CTA: read from the shared-memory list the producer warp
+// built, or (list overflow) walked with the plan iterator.
+struct ItemSource {
+  const WorkItem* list;
+  int count, k;
+  WorkIter iter;
+  __device__ __forceinline__ void init(const int32_t* hdr, const WorkItem* items, const PlanParams& plan,
+                                       const int32_t* raw, const int32_t* clamped, const int32_t* pre) {
+    list = items;
+    count = hdr[0];
+    k = 0;
+    if (count < 0) iter.init(plan, raw, clamped, pre, blockIdx.x);
+  }
+  __device__ __forceinline__ bool next(WorkItem& it) {
+    if (count >= 0) {
+      if (k >= count) return false;
+      it = list[k++];
+      return true;
+    }
+    return iter.next(it);
+  }
+};
+
 template <int HEAD_DIM, int NPAD>
 __global__ void __launch_bounds__(kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -209,6 +235,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   int32_t* s_len = reinterpret_cast<int32_t*>(misc + 512 + Cfg::kXchgBytes);  // [kMaxSmemB]
   int32_t* s_pre = s_len + kMaxSmemB;                                   // [kMaxSmemB + 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_pre + kMaxSmemB + 1);
+  // work-item list: [0] count (-1: too many, walk the iterator), [1] blocks of this CTA
+  int32_t* list_hdr = reinterpret_cast<int32_t*>(misc + 512 + Cfg::kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64);
+  WorkItem* list_items = reinterpret_cast<WorkItem*>(list_hdr + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint8_t* obuf = misc + Cfg::kMiscBytes;                                 // output rows
   float* lse_stage = reinterpret_cast<float*>(obuf + NPAD * HEAD_DIM * 4);  // [32]
@@ -287,6 +316,62 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       __threadfence_block();
     }
     __syncwarp();
+    // This CTA's work items, 32 candidates at a time (one per lane).  Owned
+    // items form a contiguous run of candidates (pairs from the first one at
+    // or after this CTA's first unit; split items c, c + C, ...).
+    {
+      const int32_t* lens_r = lens_in_smem ? s_len : p.seqlens;
+      WorkIter base_it;
+      base_it.init(plan, lens_r, s_len, s_pre, blockIdx.x);
+      const bool balanced = plan.mode == PLAN_BALANCED;
+      long long p0 = 0, total = 0;
+      if (balanced) {
+        p0 = static_cast<long long>(base_it.bal.b) * plan.kv_heads + base_it.bal.h;
+        total = static_cast<long long>(B) * plan.kv_heads;
+      } else {
+        total = static_cast<long long>(B) * plan.kv_heads * plan.num_splits;
+      }
+      int count = 0;
+      uint32_t blocks = 0;
+      for (int chunk = 0;; chunk += 32) {
+        WorkItem w;
+        bool owned = false;
+        if (balanced) {
+          const long long pr = p0 + chunk + lane;
+          if (pr < total && base_it.bal.b < B) {
+            BalancedIter bi = base_it.bal;
+            bi.b = static_cast<int>(pr / plan.kv_heads);
+            bi.h = static_cast<int>(pr - static_cast<long long>(bi.b) * plan.kv_heads);
+            // next() returns the first owned pair at or after this one: this
+            // candidate is owned iff it returns the candidate itself
+            owned = bi.next(w) && (static_cast<long long>(w.b) * plan.kv_heads + w.h == pr);
+          }
+        } else {
+          const long long wi = blockIdx.x + static_cast<long long>(chunk + lane) * plan.num_ctas;
+          if (wi < total) {
+            SplitIter si = base_it.s;
+            si.w = wi;
+            owned = si.next(w);
+          }
+        }
+        const unsigned mask = __ballot_sync(0xffffffffu, owned);
+        const int run = (~mask == 0u) ? 32 : __ffs(~mask) - 1;  // leading owned candidates
+        if (owned && lane < run) {
+          if (count + lane < kMaxListItems) list_items[count + lane] = w;
+          blocks += static_cast<uint32_t>(w.blk_end - w.blk_begin);
+        }
+        count += run;
+        if (run < 32) break;
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) blocks += __shfl_xor_sync(0xffffffffu, blocks, o);
+      if (lane == 0) {
+        list_hdr[0] = count <= kMaxListItems ? count : -1;
+        list_hdr[1] = static_cast<int32_t>(blocks);
+      }
+      __threadfence_block();
+    }
+    __syncwarp();
     if (lane == 0) ptx::mbar_arrive(BAR(PLAN_READY));
   } else {
     if (warp == 1) {
@@ -349,8 +434,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         ++t;
         return true;
       };
-      WorkIter iter;
-      iter.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
+      ItemSource iter;
+      iter.init(list_hdr, list_items, plan, lens_raw, s_len, s_pre);
       WorkItem it;
       while (ok && iter.next(it)) {
         if (it.blk_begin >= it.blk_end) continue;
@@ -404,8 +489,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       bool ok = true;
       uint32_t g = 0;  // blocks of this CTA
       int kq = 0;      // non-empty items
-      WorkIter iter;
-      iter.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
+      ItemSource iter;
+      iter.init(list_hdr, list_items, plan, lens_raw, s_len, s_pre);
       WorkItem it;
       if (is_qk) {
         constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, NPAD, 0, 0);
@@ -443,14 +528,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       } else {
         constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, Cfg::kOWidth, 1, 0);
-        // total blocks of this CTA (to find its last V tile)
-        uint32_t g_total = 0;
-        {
-          WorkIter it0;
-          it0.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
-          WorkItem w0;
-          while (it0.next(w0)) g_total += static_cast<uint32_t>(w0.blk_end - w0.blk_begin);
-        }
+        const uint32_t g_total = static_cast<uint32_t>(list_hdr[1]);  // blocks of this CTA
         while (ok && iter.next(it)) {
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
             const uint32_t sl = g & 1u;
@@ -544,14 +622,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       }
     };
 
-    // total blocks of this CTA (to locate the last V tile in the ring)
-    uint32_t g_total = 0;
-    {
-      WorkIter it0;
-      it0.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
-      WorkItem w0;
-      while (it0.next(w0)) g_total += static_cast<uint32_t>(w0.blk_end - w0.blk_begin);
-    }
+    const uint32_t g_total = static_cast<uint32_t>(list_hdr[1]);  // blocks of this CTA (last V tile)
 
     // Makes the staged rows of one item visible to the async proxy and has one
     // thread write them with bulk copies: nq copies of G contiguous rows (the
@@ -592,8 +663,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ptx::bulk_commit();
     };
 
-    WorkIter iter;
-    iter.init(plan, lens_raw, s_len, s_pre, blockIdx.x);
+    ItemSource iter;
+    iter.init(list_hdr, list_items, plan, lens_raw, s_len, s_pre);
     WorkItem it;
     uint32_t g = 0;
     bool aborted = false;

@@ -265,3 +265,31 @@ def test_split_then_merge_equals_attn():
     assert_close(out, lse, *ref, "split + merge")
     a_out, a_lse = run_gpu(inp, 0)
     assert torch.equal(out, a_out) and torch.equal(lse, a_lse)
+
+
+def _random_batch(B, s_max, nq, Hq, Hkv, d, seed, lo=0):
+    gen = torch.Generator().manual_seed(seed)
+    lens = torch.randint(lo, s_max + 1, (B,), generator=gen).to(torch.int32)
+    q = torch.randn(B, nq, Hq, d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, s_max, Hkv, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, s_max, Hkv, d, generator=gen).to(torch.bfloat16)
+    return workloads.DecodeInputs(None, q, k, v, lens, 0)
+
+
+def test_many_items_per_cta_walk_the_plan_iterator():
+    """400 sequences x 4 KV heads x 16 splits = 25600 items: more than a CTA's
+    shared-memory item list holds, so the kernel walks its plan iterator."""
+    inp = _random_batch(400, 300, 1, 8, 4, 128, seed=31)
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    out, lse = run_gpu(inp, 16, torch.float32)
+    assert_close(out, lse, *ref, "25600 split items")
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_batch_larger_than_shared_length_table(splits):
+    """600 sequences: lengths are read from global memory and the automatic
+    mode uses fixed splits."""
+    inp = _random_batch(600, 200, 2, 8, 2, 64, seed=32, lo=1)
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, causal=True)
+    out, lse = run_gpu(inp, splits, torch.bfloat16, causal=True)
+    assert_close(out, lse, *ref, f"B=600 splits={splits}")
