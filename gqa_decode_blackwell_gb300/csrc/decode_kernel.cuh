@@ -136,9 +136,16 @@ struct DecodeCfg {
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // minus alignment slack
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kSlotBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  // K and V have rings of their own (K: stages [0, kStagesK), V: the rest),
+  // each consumed in order by one issuer.  A parity wait on a stage is only
+  // sound when the waiter has itself seen the stage's previous phase complete;
+  // with one shared ring the previous tile of a stage can belong to the other
+  // consumer and still be in flight, and the wait would pass a phase early.
+  static constexpr int kStagesK = (kStages + 1) / 2;
+  static constexpr int kStagesV = kStages / 2;
   static constexpr int kRingBytes = kStages * kSlotBytes;
   static constexpr int kSmemBytes = 1024 + kRingBytes + kFixedBytes;
-  static_assert(kStages >= 4, "ring too shallow");
+  static_assert(kStages >= 4 && kStagesV >= 2, "ring too shallow");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory over budget");
   static_assert(kOWidth <= 64 && NPAD <= 32, "TMEM column plan");
   static_assert(kMiscBytes % 128 == 0 && (2 * kQBytes + 2 * kPBytes) % 128 == 0, "staging alignment");
@@ -220,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HEAD_DIM, NPAD>;
   constexpr int NS = Cfg::kStages;
+  constexpr uint32_t NSK = Cfg::kStagesK, NSV = Cfg::kStagesV;  // K ring, then V ring
   constexpr int KCH = Cfg::kChunks;
   GQA_TRACE_SETUP();
 
@@ -235,7 +243,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   int32_t* s_len = reinterpret_cast<int32_t*>(misc + 512 + Cfg::kXchgBytes);  // [kMaxSmemB]
   int32_t* s_pre = s_len + kMaxSmemB;                                   // [kMaxSmemB + 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_pre + kMaxSmemB + 1);
-  // work-item list: [0] count (-1: too many, walk the iterator), [1] blocks of this CTA
+  // work-item list: [0] count (-1: too many, walk the iterator)
   int32_t* list_hdr = reinterpret_cast<int32_t*>(misc + 512 + Cfg::kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64);
   WorkItem* list_items = reinterpret_cast<WorkItem*>(list_hdr + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -332,7 +340,6 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         total = static_cast<long long>(B) * plan.kv_heads * plan.num_splits;
       }
       int count = 0;
-      uint32_t blocks = 0;
       for (int chunk = 0;; chunk += 32) {
         WorkItem w;
         bool owned = false;
@@ -356,19 +363,11 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
         const unsigned mask = __ballot_sync(0xffffffffu, owned);
         const int run = (~mask == 0u) ? 32 : __ffs(~mask) - 1;  // leading owned candidates
-        if (owned && lane < run) {
-          if (count + lane < kMaxListItems) list_items[count + lane] = w;
-          blocks += static_cast<uint32_t>(w.blk_end - w.blk_begin);
-        }
+        if (owned && lane < run && count + lane < kMaxListItems) list_items[count + lane] = w;
         count += run;
         if (run < 32) break;
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) blocks += __shfl_xor_sync(0xffffffffu, blocks, o);
-      if (lane == 0) {
-        list_hdr[0] = count <= kMaxListItems ? count : -1;
-        list_hdr[1] = static_cast<int32_t>(blocks);
-      }
+      if (lane == 0) list_hdr[0] = count <= kMaxListItems ? count : -1;
       __threadfence_block();
     }
     __syncwarp();
@@ -412,26 +411,26 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   } else if (warp == 0) {
     if (lane == 0) {
       const uint64_t policy = ptx::l2_policy_evict_first();
-      uint32_t t = 0;   // tiles issued into the ring
+      uint32_t tk = 0, tv = 0;  // K / V tiles issued into their rings
       int kq = 0;       // non-empty items
       bool have_prev = false, ok = true;
       int pb = 0, ph = 0, pblk = 0;
-      // last tile issued per ring stage, for the drain on abort
-      [[maybe_unused]] uint32_t gk = 0, gv = 0;  // K / V blocks issued (trace indices)
-      auto load_tile = [&](const CUtensorMap* map, int b, int h, int blk) -> bool {
-        const uint32_t stage = t % NS, phase = (t / NS) & 1u;
-        if (map == &p.tm_k) GQA_TRACE_EVENT(TR_PROD_WAIT, gk);
+      auto load_tile = [&](bool is_v, int b, int h, int blk) -> bool {
+        const uint32_t n = is_v ? tv : tk;
+        const uint32_t stage = is_v ? NSK + n % NSV : n % NSK;
+        const uint32_t phase = (n / (is_v ? NSV : NSK)) & 1u;
+        if (!is_v) GQA_TRACE_EVENT(TR_PROD_WAIT, tk);
         if (!ptx::mbar_wait_bounded(BAR(RING_EMPTY + stage), phase ^ 1u, abort_flag, p.timeout_ns))
           return false;
         ptx::mbar_arrive_expect_tx(BAR(RING_FULL + stage), Cfg::kSlotBytes);
         uint8_t* dst = ring + stage * Cfg::kSlotBytes;
+        const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
 #pragma unroll
         for (int kc = 0; kc < KCH; ++kc)
           ptx::tma_load_4d_hint(ptx::smem_u32(dst + kc * 16384), map, BAR(RING_FULL + stage), kc * 64, h,
                                 blk * kBlockN, b, policy);
-        if (map == &p.tm_k) GQA_TRACE_EVENT(TR_PROD_K, gk++);
-        else GQA_TRACE_EVENT(TR_PROD_V, gv++);
-        ++t;
+        if (is_v) GQA_TRACE_EVENT(TR_PROD_V, tv++);
+        else GQA_TRACE_EVENT(TR_PROD_K, tk++);
         return true;
       };
       ItemSource iter;
@@ -453,18 +452,19 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         GQA_TRACE_EVENT(TR_PROD_Q, static_cast<uint32_t>(kq));
         ++kq;
         for (int blk = it.blk_begin; blk < it.blk_end && ok; ++blk) {
-          ok = load_tile(&p.tm_k, it.b, it.h, blk);
-          if (ok && have_prev) ok = load_tile(&p.tm_v, pb, ph, pblk);
+          ok = load_tile(false, it.b, it.h, blk);
+          if (ok && have_prev) ok = load_tile(true, pb, ph, pblk);
           pb = it.b; ph = it.h; pblk = blk; have_prev = true;
         }
       }
-      if (ok && have_prev) ok = load_tile(&p.tm_v, pb, ph, pblk);
+      if (ok && have_prev) ok = load_tile(true, pb, ph, pblk);
       if (!ok) {
         detail::set_error(kErrTimeout, abort_flag);
         // let the copies already issued land before the CTA exits
-        const uint32_t first = t > static_cast<uint32_t>(NS) ? t - NS : 0u;
-        for (uint32_t u = first; u < t; ++u)
-          ptx::mbar_wait_bounded(BAR(RING_FULL + u % NS), (u / NS) & 1u, nullptr, p.timeout_ns);
+        for (uint32_t u = tk > NSK ? tk - NSK : 0u; u < tk; ++u)
+          ptx::mbar_wait_bounded(BAR(RING_FULL + u % NSK), (u / NSK) & 1u, nullptr, p.timeout_ns);
+        for (uint32_t u = tv > NSV ? tv - NSV : 0u; u < tv; ++u)
+          ptx::mbar_wait_bounded(BAR(RING_FULL + NSK + u % NSV), (u / NSV) & 1u, nullptr, p.timeout_ns);
         for (int k = (kq > 2 ? kq - 2 : 0); k < kq; ++k)
           ptx::mbar_wait_bounded(BAR(Q_FULL + (k & 1)), (k >> 1) & 1, nullptr, p.timeout_ns);
       }
@@ -475,9 +475,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // Two single-thread issuers: warp 1 the score MMAs (QK), warp 2 the value
   // MMAs (PV).  One issuing thread alone spends ~60 cycles per tcgen05.mma
   // at these shapes; splitting the two kinds lets their issue overlap.  Each
-  // tracks its own tiles of the shared ring (order K0 K1 V0 K2 V1 ...: K of
-  // block g is tile 2g-1 (g > 0), V of block g is tile 2g+2, the CTA's last V
-  // is tile 2G-1) and releases them with its own commits.
+  // consumes its own ring in order (K of block g is K-ring tile g, V of block
+  // g is V-ring tile g; the producer issues K0 K1 V0 K2 V1 ...) and releases
+  // the stages with its own commits.
   else if (warp == 1 || warp == 2) {
     if (lane == 0) {
       const bool is_qk = (warp == 1);
@@ -504,10 +504,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           const uint64_t qd = q_desc + static_cast<uint64_t>(qb * (Cfg::kQBytes >> 4));
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
             const uint32_t sl = g & 1u;
-            const uint32_t kt = g == 0 ? 0u : 2u * g - 1u;
-            const uint32_t stage = kt % NS;
+            const uint32_t stage = g % NSK;
             ok = ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns) &&
-                 ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (kt / NS) & 1u, abort_flag, p.timeout_ns);
+                 ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSK) & 1u, abort_flag, p.timeout_ns);
             if (!ok) break;
             GQA_TRACE_EVENT(TR_MMA_K, g);
             ptx::tc_fence_after();
@@ -528,18 +527,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       } else {
         constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, Cfg::kOWidth, 1, 0);
-        const uint32_t g_total = static_cast<uint32_t>(list_hdr[1]);  // blocks of this CTA
         while (ok && iter.next(it)) {
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
             const uint32_t sl = g & 1u;
-            const uint32_t vt = (g + 1 < g_total) ? 2u * g + 2u : 2u * g + 1u;
-            const uint32_t stage = vt % NS;
+            const uint32_t stage = NSK + g % NSV;
             if (!ptx::mbar_wait_bounded(BAR(P_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns)) {
               ok = false;
               break;
             }
             GQA_TRACE_EVENT(TR_MMA_P, g);
-            if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (vt / NS) & 1u, abort_flag, p.timeout_ns)) {
+            if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSV) & 1u, abort_flag, p.timeout_ns)) {
               ok = false;
               break;
             }
@@ -621,8 +618,6 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       }
     };
-
-    const uint32_t g_total = static_cast<uint32_t>(list_hdr[1]);  // blocks of this CTA (last V tile)
 
     // Makes the staged rows of one item visible to the async proxy and has one
     // thread write them with bulk copies: nq copies of G contiguous rows (the
@@ -804,9 +799,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           const int tail_rows = L - blk * kBlockN;
           const int cap_rows = plan.max_seqlen - blk * kBlockN;
           if (tail_rows < kBlockN && cap_rows > tail_rows) {
-            const uint32_t vt = (g + 1 < g_total) ? 2u * g + 2u : 2u * g + 1u;
-            const uint32_t stage = vt % NS;
-            local_abort = !ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (vt / NS) & 1u, abort_flag, p.timeout_ns);
+            // V(g) has landed: PV(g-2) is done, so V(g - NSV) was consumed
+            // and this parity wait cannot pass a phase early.
+            const uint32_t stage = NSK + g % NSV;
+            local_abort = !ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSV) & 1u, abort_flag, p.timeout_ns);
             local_abort = __any_sync(0xffffffffu, local_abort);
             if (!local_abort && r >= tail_rows && r < cap_rows) {
 #pragma unroll
