@@ -88,7 +88,7 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 #define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event(gqa_trace_buf_, (ev), (idx))
 #else
 #define GQA_TRACE_SETUP() ((void)0)
-#define GQA_TRACE_EVENT(ev, idx) ((void)0)
+#define GQA_TRACE_EVENT(ev, idx) ((void)(idx))  // index evaluated in both builds
 #endif
 
 constexpr int kThreads = 224;       // producer, QK issuer, PV issuer, 4 softmax warps
@@ -429,8 +429,13 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         for (int kc = 0; kc < KCH; ++kc)
           ptx::tma_load_4d_hint(ptx::smem_u32(dst + kc * 16384), map, BAR(RING_FULL + stage), kc * 64, h,
                                 blk * kBlockN, b, policy);
-        if (is_v) GQA_TRACE_EVENT(TR_PROD_V, tv++);
-        else GQA_TRACE_EVENT(TR_PROD_K, tk++);
+        if (is_v) {
+          GQA_TRACE_EVENT(TR_PROD_V, tv);
+          ++tv;
+        } else {
+          GQA_TRACE_EVENT(TR_PROD_K, tk);
+          ++tk;
+        }
         return true;
       };
       ItemSource iter;
@@ -799,8 +804,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           const int tail_rows = L - blk * kBlockN;
           const int cap_rows = plan.max_seqlen - blk * kBlockN;
           if (tail_rows < kBlockN && cap_rows > tail_rows) {
-            // V(g) has landed: PV(g-2) is done, so V(g - NSV) was consumed
-            // and this parity wait cannot pass a phase early.
+            // Wait for V(g) to land.  PV(g-2) is done, so V(g - NSV) was
+            // consumed and this parity wait cannot pass a phase early.
             const uint32_t stage = NSK + g % NSV;
             local_abort = !ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSV) & 1u, abort_flag, p.timeout_ns);
             local_abort = __any_sync(0xffffffffu, local_abort);
