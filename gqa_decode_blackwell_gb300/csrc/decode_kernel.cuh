@@ -130,12 +130,17 @@ struct DecodeCfg {
   static constexpr int kListBytes = 16 + kMaxListItems * static_cast<int>(sizeof(WorkItem));
   static constexpr int kMiscBytes =
       (512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64 + kListBytes + 127) / 128 * 128;
-  // output staging: one item's rows (fp32 worst case), its LSEs, its piece count
-  static constexpr int kOutBytes = NPAD * HEAD_DIM * 4 + 128 + 16;
-  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes + kOutBytes;
+  // output staging, two buffers: one item's rows (fp32 worst case), its LSEs,
+  // its piece count
+  static constexpr int kOutBytes = (NPAD * HEAD_DIM * 4 + 128 + 16 + 127) / 128 * 128;
+  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes + 2 * kOutBytes;
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // minus alignment slack
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kSlotBytes;
-  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  // Four stages (two K, two V blocks) per SM keep enough bytes in flight
+  // for the whole GPU (152 x 64-128 KB, about twice the bandwidth-latency
+  // product); deeper rings were measured slower: the extra queueing made the
+  // per-SM bandwidth less even and the slowest CTA later.
+  static constexpr int kStages = kStagesRaw > 4 ? 4 : kStagesRaw;
   // K and V have rings of their own (K: stages [0, kStagesK), V: the rest),
   // each consumed in order by one issuer.  A parity wait on a stage is only
   // sound when the waiter has itself seen the stage's previous phase complete;
@@ -247,9 +252,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   int32_t* list_hdr = reinterpret_cast<int32_t*>(misc + 512 + Cfg::kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64);
   WorkItem* list_items = reinterpret_cast<WorkItem*>(list_hdr + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint8_t* obuf = misc + Cfg::kMiscBytes;                                 // output rows
-  float* lse_stage = reinterpret_cast<float*>(obuf + NPAD * HEAD_DIM * 4);  // [32]
-  int32_t* np_stage = reinterpret_cast<int32_t*>(lse_stage + 32);         // [4]
+  // output staging buffer ob: rows, then 32 LSEs, then the piece count
+  auto obuf_of = [&](int ob) -> uint8_t* { return misc + Cfg::kMiscBytes + ob * Cfg::kOutBytes; };
+  auto lse_of = [&](int ob) -> float* { return reinterpret_cast<float*>(obuf_of(ob) + NPAD * HEAD_DIM * 4); };
+  auto np_of = [&](int ob) -> int32_t* { return reinterpret_cast<int32_t*>(lse_of(ob) + 32); };
 
   // barrier indices
   const uint32_t bar_base = ptx::smem_u32(bar);
@@ -268,7 +274,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // the plan itself right after the grid dependency, publishes it through
   // PLAN_READY and starts streaming, while the other warps allocate TMEM and
   // zero the padding of the MMA operand buffers.
-  const int PLAN_READY = DRAIN + 2;
+  const int PLAN_READY = DRAIN + 2, OUT_FULL = DRAIN + 3, OUT_EMPTY = DRAIN + 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       ptx::mbar_init(BAR(RING_FULL + i), 1);
@@ -285,6 +291,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     ptx::mbar_init(BAR(DRAIN), 1);
     ptx::mbar_init(BAR(DRAIN + 1), 1);
     ptx::mbar_init(BAR(PLAN_READY), 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(BAR(OUT_FULL + i), 1);
+      ptx::mbar_init(BAR(OUT_EMPTY + i), 1);
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&p.tm_q);
@@ -295,6 +305,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 
   uint32_t tmem_base = 0;
   if (warp == 0) {
+    // Warm L2 with the lengths while the previous kernel finishes: a prefetch
+    // returns no data, so it cannot observe a value that kernel still writes.
+    if (lens_in_smem && lane * 32 < B) ptx::prefetch_l2(p.seqlens + lane * 32);
     // Inputs may be produced by the previous kernel in the stream.
     ptx::griddep_wait();
     if (lane == 0) GQA_TRACE_EVENT(TR_START, 0);
@@ -330,7 +343,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     {
       const int32_t* lens_r = lens_in_smem ? s_len : p.seqlens;
       WorkIter base_it;
-      base_it.init(plan, lens_r, s_len, s_pre, blockIdx.x);
+      base_it.init_warp(plan, lens_r, s_len, s_pre, blockIdx.x, lane);
       const bool balanced = plan.mode == PLAN_BALANCED;
       long long p0 = 0, total = 0;
       if (balanced) {
@@ -405,6 +418,52 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   const bool plan_ok = (warp == 0) || (*abort_flag == 0);
   const int32_t* lens_raw = lens_in_smem ? s_len : p.seqlens;
 
+  // Who issues an item's output copies.  Issuing a bulk copy can wait behind
+  // the SM's queued TMA loads for hundreds of cycles.  With 32 columns the
+  // softmax warpgroup is the bottleneck, and the value-MMA thread (idle while
+  // the softmax warpgroup finishes an item) issues them.  With 16 columns the
+  // KV stream is the bottleneck and the first softmax thread issues them
+  // itself: measured on GB300, that build's softmax loop runs faster.
+  constexpr bool kPvStores = (NPAD == 32);
+
+  // Writes item wi's rows from staging buffer ob with bulk copies: nq copies
+  // of G contiguous rows (the G query heads of one token) for O, the same for
+  // the LSEs and, for the first piece of a balanced-plan pair, its piece
+  // count.
+  auto store_item = [&](const WorkItem& wi, int ob) {
+    const int rows_total = plan.batch * p.nq * p.Hq;
+    const long long pair_idx = static_cast<long long>(wi.b) * plan.kv_heads + wi.h;
+    const bool with_o = wi.blk_begin < wi.blk_end;  // an empty split publishes only lse = -inf
+    const bool final_out = wi.slot < 0;
+    const uint32_t esz = (final_out && !p.out_fp32) ? 2u : 4u;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.G) * HEAD_DIM * esz;
+    const float* lse_st = lse_of(ob);
+    for (int t = 0; t < p.nq; ++t) {
+      const long long row0 = (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G;
+      if (final_out || with_o) {
+        uint8_t* dst = final_out
+            ? static_cast<uint8_t*>(p.out) + row0 * HEAD_DIM * esz
+            : reinterpret_cast<uint8_t*>(p.o_part + (static_cast<long long>(wi.slot) * rows_total + row0) * HEAD_DIM);
+        ptx::bulk_store(dst, ptx::smem_u32(obuf_of(ob) + static_cast<uint32_t>(t) * row_bytes), row_bytes);
+      }
+      float* lse_dst = final_out ? (p.lse != nullptr ? p.lse + row0 : nullptr)
+                                 : p.lse_part + static_cast<long long>(wi.slot) * rows_total + row0;
+      if (lse_dst != nullptr) {
+        if (p.lse_bulk) {
+          ptx::bulk_store(lse_dst, ptx::smem_u32(lse_st + t * p.G), static_cast<uint32_t>(p.G) * 4u);
+        } else {
+          for (int g2 = 0; g2 < p.G; ++g2) lse_dst[g2] = lse_st[t * p.G + g2];
+        }
+      }
+    }
+    if (wi.first_piece && p.n_pieces != nullptr) {
+      np_of(ob)[0] = wi.n_pieces;
+      ptx::fence_proxy_async_smem();
+      ptx::bulk_store(p.n_pieces + pair_idx * 4, ptx::smem_u32(np_of(ob)), 16u);
+    }
+    ptx::bulk_commit();
+  };
+
   // =============================================================== producer
   if (!plan_ok) {
     // the plan never arrived: nothing was issued, go straight to teardown
@@ -420,7 +479,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         const uint32_t stage = is_v ? NSK + n % NSV : n % NSK;
         const uint32_t phase = (n / (is_v ? NSV : NSK)) & 1u;
         if (!is_v) GQA_TRACE_EVENT(TR_PROD_WAIT, tk);
-        if (!ptx::mbar_wait_bounded(BAR(RING_EMPTY + stage), phase ^ 1u, abort_flag, p.timeout_ns))
+        // the first pass over a ring needs no wait: a fresh barrier's
+        // preceding phase counts as complete
+        if (n >= (is_v ? NSV : NSK) &&
+            !ptx::mbar_wait_bounded(BAR(RING_EMPTY + stage), phase ^ 1u, abort_flag, p.timeout_ns))
           return false;
         ptx::mbar_arrive_expect_tx(BAR(RING_FULL + stage), Cfg::kSlotBytes);
         uint8_t* dst = ring + stage * Cfg::kSlotBytes;
@@ -445,7 +507,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (it.blk_begin >= it.blk_end) continue;
         GQA_TRACE_EVENT(TR_PROD_PLAN, static_cast<uint32_t>(kq));
         const int qb = kq & 1;
-        if (!ptx::mbar_wait_bounded(BAR(Q_EMPTY + qb), ((kq >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
+        if (kq >= 2 && !ptx::mbar_wait_bounded(BAR(Q_EMPTY + qb), ((kq >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -510,7 +572,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
             const uint32_t sl = g & 1u;
             const uint32_t stage = g % NSK;
-            ok = ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns) &&
+            ok = (g < 2 || ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns)) &&
                  ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSK) & 1u, abort_flag, p.timeout_ns);
             if (!ok) break;
             GQA_TRACE_EVENT(TR_MMA_K, g);
@@ -532,6 +594,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       } else {
         constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, Cfg::kOWidth, 1, 0);
+        uint32_t k = 0;  // items
         while (ok && iter.next(it)) {
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
             const uint32_t sl = g & 1u;
@@ -568,7 +631,28 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
             ptx::mma_commit(BAR(RING_EMPTY + stage));
             GQA_TRACE_EVENT(TR_MMA_PV, g);
           }
+          if (!ok) break;
+          if constexpr (kPvStores) {
+            // The softmax warpgroup hands over this item's staged rows before
+            // it sends the next item's first P, so nothing is delayed by
+            // waiting here.  Once this item's copies are issued, the previous
+            // item's copies have read their buffer and it can be reused.
+            const int ob = static_cast<int>(k & 1u);
+            if (!ptx::mbar_wait_bounded(BAR(OUT_FULL + ob), (k >> 1) & 1u, abort_flag, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            store_item(it, ob);
+            if (k >= 1) {
+              ptx::bulk_wait_read_all_but_last();
+              ptx::mbar_arrive(BAR(OUT_EMPTY + (ob ^ 1)));
+            }
+          }
+          ++k;
         }
+        ptx::bulk_wait_all();  // this CTA's outputs are in global memory
+        GQA_TRACE_EVENT(TR_SM_E1, 0);
+        ptx::griddep_launch_dependents();
       }
       if (!ok) detail::set_error(kErrTimeout, abort_flag);
       // every MMA this thread issued has completed before TMEM is released
@@ -584,7 +668,6 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int r = tq * 32 + lane;     // TMEM lane = KV row of S^T = row of O^T
     const uint32_t lane_addr = static_cast<uint32_t>(tq * 32) << 16;
     const int nv = p.nq * p.G;        // valid columns
-    const int rows_total = plan.batch * p.nq * p.Hq;
     bool local_abort = false;
     uint32_t xc = 0;                  // exchange counter
 
@@ -624,43 +707,31 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       }
     };
 
-    // Makes the staged rows of one item visible to the async proxy and has one
-    // thread write them with bulk copies: nq copies of G contiguous rows (the
-    // G query heads of one token) for O, the same for the LSEs, and (balanced
-    // plan) the pair's piece count.  A plain global store could wait behind
-    // the in-flight TMA loads of this SM for microseconds and hold the whole
-    // warpgroup; the bulk copies are asynchronous.
-    auto issue_outputs = [&](const WorkItem& wi, long long pair_idx, bool with_o) {
+    // Staging buffer of the next item: free once the copies of the item two
+    // before it have read it.  Thread 0 of the warpgroup waits; the result
+    // joins the next exchange's flags.
+    uint32_t k_out = 0;  // items staged
+    auto wait_staging = [&]() -> bool {
+      if (threadIdx.x != kSoftmaxThread0) return true;
+      if constexpr (!kPvStores) {
+        ptx::bulk_wait_read_all();
+        return true;
+      } else {
+        if (k_out < 2) return true;
+        return ptx::mbar_wait_bounded(BAR(OUT_EMPTY + (k_out & 1u)), ((k_out >> 1) & 1u) ^ 1u, abort_flag,
+                                      p.timeout_ns);
+      }
+    };
+    // Makes the staged rows visible to the async proxy and writes them out
+    // (or hands them to the value-MMA thread).
+    auto hand_over = [&](const WorkItem& wi) {
       ptx::fence_proxy_async_smem();
       ptx::named_barrier_sync(1, 128);
-      if (threadIdx.x != kSoftmaxThread0) return;
-      const bool final_out = wi.slot < 0;
-      const uint32_t esz = (final_out && !p.out_fp32) ? 2u : 4u;
-      const uint32_t row_bytes = static_cast<uint32_t>(p.G) * HEAD_DIM * esz;
-      for (int t = 0; t < p.nq; ++t) {
-        const long long row0 = (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G;
-        if (final_out || with_o) {
-          uint8_t* dst = final_out
-              ? static_cast<uint8_t*>(p.out) + row0 * HEAD_DIM * esz
-              : reinterpret_cast<uint8_t*>(p.o_part + (static_cast<long long>(wi.slot) * rows_total + row0) * HEAD_DIM);
-          ptx::bulk_store(dst, ptx::smem_u32(obuf + static_cast<uint32_t>(t) * row_bytes), row_bytes);
-        }
-        float* lse_dst = final_out ? (p.lse != nullptr ? p.lse + row0 : nullptr)
-                                   : p.lse_part + static_cast<long long>(wi.slot) * rows_total + row0;
-        if (lse_dst != nullptr) {
-          if (p.lse_bulk) {
-            ptx::bulk_store(lse_dst, ptx::smem_u32(lse_stage + t * p.G), static_cast<uint32_t>(p.G) * 4u);
-          } else {
-            for (int g2 = 0; g2 < p.G; ++g2) lse_dst[g2] = lse_stage[t * p.G + g2];
-          }
-        }
+      if (threadIdx.x == kSoftmaxThread0) {
+        if constexpr (kPvStores) ptx::mbar_arrive(BAR(OUT_FULL + (k_out & 1u)));
+        else store_item(wi, static_cast<int>(k_out & 1u));
       }
-      if (wi.first_piece && p.n_pieces != nullptr) {
-        np_stage[0] = wi.n_pieces;
-        ptx::fence_proxy_async_smem();
-        ptx::bulk_store(p.n_pieces + pair_idx * 4, ptx::smem_u32(np_stage), 16u);
-      }
-      ptx::bulk_commit();
+      ++k_out;
     };
 
     ItemSource iter;
@@ -669,22 +740,21 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     uint32_t g = 0;
     bool aborted = false;
     while (!aborted && iter.next(it)) {
-      const int b = it.b, h = it.h;
-      const long long pair = static_cast<long long>(b) * plan.kv_heads + h;
       if (it.blk_begin >= it.blk_end) {
         // empty item: final output O = 0, lse = -inf; partial lse = -inf
-        if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_read_all();
-        ptx::named_barrier_sync(1, 128);  // staging free
+        const bool st_ok = wait_staging();
+        if (exchange(st_ok ? 0u : 2u, false, 0.f) & 2u) { aborted = true; break; }
+        uint8_t* ob = obuf_of(static_cast<int>(k_out & 1u));
         if (r < HEAD_DIM) {
           for (int n = 0; n < nv; ++n) {
             if (it.slot < 0 && !p.out_fp32)
-              reinterpret_cast<__nv_bfloat16*>(obuf)[n * HEAD_DIM + r] = __float2bfloat16_rn(0.f);
+              reinterpret_cast<__nv_bfloat16*>(ob)[n * HEAD_DIM + r] = __float2bfloat16_rn(0.f);
             else
-              reinterpret_cast<float*>(obuf)[n * HEAD_DIM + r] = 0.f;
+              reinterpret_cast<float*>(ob)[n * HEAD_DIM + r] = 0.f;
           }
         }
-        if (r < nv) lse_stage[r] = -INFINITY;
-        issue_outputs(it, pair, false);
+        if (r < nv) lse_of(static_cast<int>(k_out & 1u))[r] = -INFINITY;
+        hand_over(it);
         continue;
       }
       const int L = it.L;
@@ -786,7 +856,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           l[n] += pr[n];
         }
         // P buffer sl is free once PV(g-2) has completed
-        if (!local_abort)
+        if (!local_abort && g >= 2)
           local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns);
         local_abort = __any_sync(0xffffffffu, local_abort);
         if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_PE, g);
@@ -834,8 +904,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag, p.timeout_ns);
       local_abort = __any_sync(0xffffffffu, local_abort);
       const float lsum = detail::transpose_reduce<NPAD, false>(l, lane);
-      if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_read_all();  // staging free after f3
-      const uint32_t f3 = exchange(local_abort ? 2u : 0u, true, lsum);
+      const bool st_ok = wait_staging();  // staging buffer free after f3
+      const uint32_t f3 = exchange((local_abort || !st_ok) ? 2u : 0u, true, lsum);
       if (f3 & 2u) { aborted = true; break; }
       float lt[NPAD];
       xcombine(lt, false);
@@ -870,9 +940,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         writer = r < 64;
       }
       // Outputs go to shared memory in their global layout (row n = t*G + g
-      // of this pair, d contiguous) and leave by bulk copies (issue_outputs).
+      // of this pair, d contiguous); the output warp writes them out.
       if (writer) {
         const bool as_bf16 = it.slot < 0 && !p.out_fp32;
+        uint8_t* obuf = obuf_of(static_cast<int>(k_out & 1u));
 #pragma unroll
         for (int n = 0; n < NPAD; ++n) {
           const float inv = lt[n] > 0.f ? ptx::rcp_approx(lt[n]) : 0.f;
@@ -887,17 +958,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
           for (int n = 0; n < NPAD; ++n)
             if (n == d_row) { lt_n = lt[n]; m_n = m[n]; }
-          lse_stage[d_row] = lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
+          lse_of(static_cast<int>(k_out & 1u))[d_row] =
+              lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
         }
       }
-      issue_outputs(it, pair, true);
+      hand_over(it);
     }
-    if (threadIdx.x == kSoftmaxThread0) {
-      ptx::bulk_wait_all();  // this CTA's outputs are in global memory
-      GQA_TRACE_EVENT(TR_SM_E1, g);
+    if constexpr (!kPvStores) {
+      if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_all();  // this CTA's outputs are in global memory
     }
     if (aborted || local_abort) detail::set_error(kErrTimeout, abort_flag);
-    // results of this CTA are written: dependents may launch
     ptx::griddep_launch_dependents();
   }
 

@@ -141,15 +141,50 @@ struct BalancedIter {
     }
     lo = muldiv(c, U, C);
     hi = muldiv(c + 1, U, C);
-    // first pair: smallest b whose units end after lo, or that starts at or after lo
+    // first pair: the smallest b that reaches lo (the predicate is monotone in b)
     int a = 0, z = B;
     while (a < z) {
       const int mid = (a + z) / 2;
-      const bool ok = static_cast<long long>(H) * pre[mid + 1] > lo ||
-                      static_cast<long long>(H) * pre[mid] >= lo;
-      if (ok) z = mid; else a = mid + 1;
+      if (reaches(mid)) z = mid; else a = mid + 1;
     }
     b = a;
+    set_first_head();
+  }
+#ifdef __CUDACC__
+  // The same result as init(), computed by the 32 lanes of a warp together:
+  // lo and hi in two lanes at once, and the first pair by a ballot over 32
+  // sequences at a time instead of a serial binary search.  Every lane must
+  // call it; every lane ends with the same state.
+  __device__ __forceinline__ void init_warp(const PlanParams& p, const int32_t* l, const int32_t* prefix, int c,
+                                            int lane) {
+    lens = l; pre = prefix; cta = c;
+    B = p.batch; H = p.kv_heads;
+    U = static_cast<long long>(H) * pre[B];
+    C = U <= 0 ? 1 : (U < p.num_ctas ? static_cast<int>(U) : p.num_ctas);
+    if (c >= C) {
+      b = B; h = 0; lo = hi = U;
+      return;
+    }
+    const long long v = muldiv(c + (lane & 1), U, C);
+    lo = __shfl_sync(0xffffffffu, v, 0);
+    hi = __shfl_sync(0xffffffffu, v, 1);
+    b = B;
+    for (int base = 0; base < B; base += 32) {
+      const unsigned m = __ballot_sync(0xffffffffu, base + lane < B && reaches(base + lane));
+      if (m != 0u) {
+        b = base + __ffs(m) - 1;
+        break;
+      }
+    }
+    set_first_head();
+  }
+#endif
+  // Sequence b holds a unit at or after lo, or starts at or after lo.
+  GQA_HD bool reaches(int bb) const {
+    return static_cast<long long>(H) * pre[bb + 1] > lo || static_cast<long long>(H) * pre[bb] >= lo;
+  }
+  // First head of the first pair: the head whose units contain lo.
+  GQA_HD void set_first_head() {
     h = 0;
     if (b < B) {
       const long long start = static_cast<long long>(H) * pre[b];
@@ -208,6 +243,15 @@ struct WorkIter {
     if (mode == PLAN_BALANCED) bal.init(p, clamped_lens, prefix, cta);
     else s.init(p, raw_lens, cta);
   }
+#ifdef __CUDACC__
+  // Warp-cooperative init (all 32 lanes), same result as init().
+  __device__ __forceinline__ void init_warp(const PlanParams& p, const int32_t* raw_lens,
+                                            const int32_t* clamped_lens, const int32_t* prefix, int cta, int lane) {
+    mode = p.mode;
+    if (mode == PLAN_BALANCED) bal.init_warp(p, clamped_lens, prefix, cta, lane);
+    else s.init(p, raw_lens, cta);
+  }
+#endif
   GQA_HD bool next(WorkItem& it) { return mode == PLAN_BALANCED ? bal.next(it) : s.next(it); }
 };
 

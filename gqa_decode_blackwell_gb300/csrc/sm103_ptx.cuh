@@ -56,13 +56,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits until the phase with the given parity has completed.  Returns false
 // (without having observed completion) when `*abort_flag` becomes non-zero or
 // when `timeout_ns` of wall time pass; the caller then records the error.
+// try_wait with a suspend-time hint: the thread may be suspended for up to
+// hint_ns while the phase is incomplete, instead of polling.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// suspend_hint_ns > 0: waits with suspended tries (for waiters whose latency
+// matters little, so that they take fewer issue slots from the warps they
+// share a scheduler with).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort_flag,
-                                                  uint64_t timeout_ns) {
+                                                  uint64_t timeout_ns, uint32_t suspend_hint_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (suspend_hint_ns != 0 ? mbar_try_wait_hint(bar, parity, suspend_hint_ns) : mbar_try_wait(bar, parity))
+      return true;
     if ((it & 63u) == 0u) {
       if (abort_flag != nullptr && *abort_flag != 0) return false;
       if (globaltimer_ns() - t0 > timeout_ns) return false;
@@ -88,6 +106,10 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -136,6 +158,11 @@ __device__ __forceinline__ void bulk_commit() {
 // its shared-memory source.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until all but the most recent committed bulk group of this thread
+// have finished reading their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read_all_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {

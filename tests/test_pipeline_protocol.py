@@ -9,7 +9,10 @@ with c = k + 2 it blocks on a phase that has already completed.
 This module replays the protocol of one CTA (producer, score-MMA issuer,
 value-MMA issuer, softmax warpgroup) under random interleavings: TMA loads land
 in any order, the MMAs of one issuing thread complete in issue order, each
-agent advances whenever its wait is satisfied.  Every wait is checked against
+agent advances whenever its wait is satisfied.  A CTA's blocks belong to work
+items (some empty); at the end of each item the softmax warpgroup hands a
+staging buffer (two of them, OUT_FULL / OUT_EMPTY) to the value-MMA thread,
+which writes the item out and releases the previous item's buffer.  Every wait is checked against
 the rule above.  The K/V ring layout is a parameter so that the check also
 shows why K and V need rings of their own: with one shared ring whose depth
 is odd, a stage's previous tile can belong to the other issuer and still be
@@ -55,9 +58,14 @@ def shared_ring(ns):
     return k_slot, v_slot
 
 
-def run_cta(ns, G, layout, rng, tail_wait=True):
-    """One CTA with G blocks; raises Violation on an unsound parity wait."""
+def run_cta(ns, G, layout, rng, tail_wait=True, items=None):
+    """One CTA with G blocks in `items` (block counts, default one item);
+    raises Violation on an unsound parity wait or a deadlock."""
+    if items is None:
+        items = [G]
+    assert sum(items) == G
     k_slot, v_slot = layout(ns)
+    out_full, out_empty = [Bar(), Bar()], [Bar(), Bar()]
     ring_full = [Bar() for _ in range(ns)]
     ring_empty = [Bar() for _ in range(ns)]
     s_full, s_empty = [Bar(), Bar()], [Bar(), Bar()]
@@ -108,25 +116,41 @@ def run_cta(ns, G, layout, rng, tail_wait=True):
             mma_q["qk"].append(ring_empty[stage])
 
     def pv():
-        for g in range(G):
-            sl = g & 1
-            yield from wait(p_full[sl], g >> 1, f"pv P_FULL {g}")
-            stage, ph = v_slot(g, G)
-            yield from wait(ring_full[stage], ph, f"pv RING_FULL V{g}")
-            mma_q["pv"].append(p_empty[sl])
-            mma_q["pv"].append(ring_empty[stage])
+        g = 0
+        for k, nb in enumerate(items):
+            for _ in range(nb):
+                sl = g & 1
+                yield from wait(p_full[sl], g >> 1, f"pv P_FULL {g}")
+                stage, ph = v_slot(g, G)
+                yield from wait(ring_full[stage], ph, f"pv RING_FULL V{g}")
+                mma_q["pv"].append(p_empty[sl])
+                mma_q["pv"].append(ring_empty[stage])
+                g += 1
+            # write item k out; item k-1's buffer has been read
+            yield from wait(out_full[k & 1], k >> 1, f"pv OUT_FULL item {k}")
+            if k >= 1:
+                out_empty[(k - 1) & 1].c += 1
 
     def softmax():
-        for g in range(G):
-            sl = g & 1
-            yield from wait(s_full[sl], g >> 1, f"softmax S_FULL {g}")
-            s_empty[sl].c += 1
-            if g >= 2:
-                yield from wait(p_empty[sl], (g >> 1) - 1, f"softmax P_EMPTY {g}")
-            if tail_wait:  # zeroing the rows of V past the sequence end
-                stage, ph = v_slot(g, G)
-                yield from wait(ring_full[stage], ph, f"softmax tail V{g}")
-            p_full[sl].c += 1
+        g = 0
+        for k, nb in enumerate(items):
+            for _ in range(nb):
+                sl = g & 1
+                yield from wait(s_full[sl], g >> 1, f"softmax S_FULL {g}")
+                s_empty[sl].c += 1
+                if g >= 2:
+                    yield from wait(p_empty[sl], (g >> 1) - 1, f"softmax P_EMPTY {g}")
+                if tail_wait:  # zeroing the rows of V past the sequence end
+                    stage, ph = v_slot(g, G)
+                    yield from wait(ring_full[stage], ph, f"softmax tail V{g}")
+                p_full[sl].c += 1
+                g += 1
+            if nb > 0:  # epilogue: the item's last value MMA has completed
+                gl = g - 1
+                yield from wait(p_empty[gl & 1], gl >> 1, f"softmax epilogue P_EMPTY {gl}")
+            if k >= 2:  # staging buffer of item k-2 released
+                yield from wait(out_empty[k & 1], (k >> 1) - 1, f"softmax OUT_EMPTY item {k}")
+            out_full[k & 1].c += 1
 
     agents = {"producer": producer(), "qk": qk(), "pv": pv(), "softmax": softmax()}
     live = dict(agents)
@@ -156,6 +180,32 @@ def test_split_rings_sound(ns):
     rng = random.Random(1000 + ns)
     for trial in range(600):
         run_cta(ns, rng.randint(1, 12), split_rings, rng)
+
+
+def random_items(rng, G):
+    """G blocks cut into items, with empty items mixed in."""
+    items, left = [], G
+    while left > 0 or rng.random() < 0.2:
+        if rng.random() < 0.15:
+            items.append(0)
+            continue
+        nb = rng.randint(1, max(1, left)) if left > 0 else 0
+        items.append(nb)
+        left -= nb
+        if left == 0 and rng.random() < 0.7:
+            break
+    return items
+
+
+@pytest.mark.parametrize("ns", [4, 5, 6, 12])
+def test_item_handoff_sound(ns):
+    """Several items per CTA, empty ones included: staging handoff and the
+    epilogue's wait on the last value MMA stay sound and free of deadlock."""
+    rng = random.Random(77 + ns)
+    for trial in range(500):
+        G = rng.randint(0, 12)
+        items = random_items(rng, G)
+        run_cta(ns, G, split_rings, rng, items=items)
 
 
 def test_shared_ring_with_odd_depth_is_unsound():
