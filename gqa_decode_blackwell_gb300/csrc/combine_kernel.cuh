@@ -12,6 +12,8 @@
 //
 // One warp per row; each lane owns 4 (head_dim 128) or 2 (head_dim 64)
 // consecutive output elements, read as one 16- or 8-byte vector per split.
+// Up to 64 splits the LSEs stay in two registers per lane; more splits (a
+// long sequence cut over many CTAs) take a two-pass loop over groups of 32.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -21,24 +23,39 @@
 namespace gqa {
 
 constexpr int kCombineThreads = 256;
-constexpr int kMaxSplits = 64;
 
 struct CombineParams {
-  const float* o_part;      // [num_slots, rows, d]
-  const float* lse_part;    // [num_slots, rows]
+  const float* o_part;      // [num_splits, rows, d]
+  const float* lse_part;    // [num_splits, rows]
   const int32_t* n_pieces;  // optional [B * Hkv][4]: valid slots per pair in [0] (balanced plan)
   void* out;                // [rows, d] bf16 or fp32
   float* lse;               // [rows] or null
   long long rows;
-  int num_splits;           // slots to merge when n_pieces is null
+  int num_splits;           // slots per row (all of them are merged when n_pieces is null)
   int out_fp32;
   int nq, Hq, G, kv_heads;  // row -> pair mapping for n_pieces
 };
+
+namespace detail {
+
+template <int VEC>
+__device__ __forceinline__ void load_vec(const float* src, float (&v)[VEC]) {
+  if constexpr (VEC == 4) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else {
+    const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+    v[0] = x.x; v[1] = x.y;
+  }
+}
+
+}  // namespace detail
 
 template <int HEAD_DIM>
 __global__ void __launch_bounds__(kCombineThreads)
 gqa_combine_kernel(const CombineParams p) {
   constexpr int VEC = HEAD_DIM / 32;  // elements per lane
+  constexpr float kLog2e = 1.4426950408889634f;
   // Partials come from the preceding decode launch.
   ptx::griddep_wait();
 
@@ -46,86 +63,118 @@ gqa_combine_kernel(const CombineParams p) {
   const long long row = static_cast<long long>(blockIdx.x) * (kCombineThreads / 32) + (threadIdx.x >> 5);
   if (row >= p.rows) return;
 
-  // Every load below is independent of the others, so they are all issued
-  // before the first use: the piece count, the LSEs of every allocated slot
-  // and the first kSpec partial rows.  Slots beyond the valid count are
-  // allocated memory whose values are masked out, never used.
-  constexpr int kSpec = 4;
-  const int slots = p.num_splits;  // allocated slots
-  int n = slots;
-  const int* np_ptr = nullptr;
+  // split s of this row is partial row first + s * stride
+  const long long first = row, stride = p.rows;
+  int n = p.num_splits;
+  const int32_t* rec = nullptr;
   if (p.n_pieces != nullptr) {
-    const long long bt = row / p.Hq;            // b * nq + t
+    const long long bt = row / p.Hq;  // b * nq + t
     const int hq = static_cast<int>(row % p.Hq);
     const long long b = bt / p.nq;
-    np_ptr = p.n_pieces + (b * p.kv_heads + hq / p.G) * 4;  // one 16-byte record per pair
+    rec = p.n_pieces + (b * p.kv_heads + hq / p.G) * 4;  // one 16-byte record per pair
   }
-  const int n_raw = np_ptr != nullptr ? *np_ptr : slots;
-  float l0 = lane < slots ? p.lse_part[static_cast<long long>(lane) * p.rows + row] : -INFINITY;
-  float l1 = lane + 32 < slots ? p.lse_part[static_cast<long long>(lane + 32) * p.rows + row] : -INFINITY;
-  float spec[kSpec][VEC];
+  constexpr int kSpec = 4;
+  float l0, l1, spec[kSpec][VEC];
+  auto lse_at = [&](int s) -> float { return p.lse_part[first + s * stride]; };
+  auto o_at = [&](int s) -> const float* { return p.o_part + (first + s * stride) * HEAD_DIM + lane * VEC; };
+  auto load_fast = [&](int slots) {
+    // Up to 64 slots: the LSEs of every slot and the first kSpec partial
+    // rows, all issued before the first use.  Slots past the valid count
+    // are masked out, never used.
+    l0 = lane < slots ? lse_at(lane) : -INFINITY;
+    l1 = lane + 32 < slots ? lse_at(lane + 32) : -INFINITY;
 #pragma unroll
-  for (int s = 0; s < kSpec; ++s) {
-    if (s < slots) {
-      const float* src = p.o_part + (static_cast<long long>(s) * p.rows + row) * HEAD_DIM + lane * VEC;
-      if constexpr (VEC == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-        spec[s][0] = v.x; spec[s][1] = v.y; spec[s][2] = v.z; spec[s][3] = v.w;
+    for (int s = 0; s < kSpec; ++s) {
+      if (s < slots) {
+        detail::load_vec<VEC>(o_at(s), spec[s]);
       } else {
-        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
-        spec[s][0] = v.x; spec[s][1] = v.y;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) spec[s][i] = 0.f;
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) spec[s][i] = 0.f;
     }
+  };
+  {
+    // the addresses do not depend on the piece count, so the loads go out
+    // together with it
+    const int slots = p.num_splits;
+    const int n_raw = rec != nullptr ? *rec : slots;
+    const bool loaded = slots <= 64;
+    if (loaded) load_fast(slots);
+    if (rec != nullptr) {
+      n = n_raw < slots ? n_raw : slots;
+      if (n <= 1) return;  // written directly by the decode kernel
+    }
+    if (!loaded && n <= 64) load_fast(n);
   }
-  if (np_ptr != nullptr) {
-    n = n_raw < slots ? n_raw : slots;
-    if (n <= 1) return;                          // written directly by the decode kernel
-  }
-  if (lane >= n) l0 = -INFINITY;
-  if (lane + 32 >= n) l1 = -INFINITY;
-  float M = fmaxf(l0, l1);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
   float acc[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
   float lse_out = -INFINITY;
 
-  if (M != -INFINITY) {
-    constexpr float kLog2e = 1.4426950408889634f;
-    const float w0 = l0 == -INFINITY ? 0.f : ptx::ex2_approx((l0 - M) * kLog2e);
-    const float w1 = l1 == -INFINITY ? 0.f : ptx::ex2_approx((l1 - M) * kLog2e);
-    float W = w0 + w1;
+  if (n <= 64) {
+    if (lane >= n) l0 = -INFINITY;
+    if (lane + 32 >= n) l1 = -INFINITY;
+    float M = fmaxf(l0, l1);
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M != -INFINITY) {
+      const float w0 = l0 == -INFINITY ? 0.f : ptx::ex2_approx((l0 - M) * kLog2e);
+      const float w1 = l1 == -INFINITY ? 0.f : ptx::ex2_approx((l1 - M) * kLog2e);
+      float W = w0 + w1;
 #pragma unroll
-    for (int s = 0; s < kSpec; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w0, s);
-      if (s < n && ws != 0.f) {
+      for (int o = 16; o >= 1; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) acc[i] += ws * spec[s][i];
+      for (int s = 0; s < kSpec; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, w0, s);
+        if (s < n && ws != 0.f) {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) acc[i] += ws * spec[s][i];
+        }
       }
-    }
-    for (int s = kSpec; s < n; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      if (ws == 0.f) continue;  // empty split (or a weight that underflows): not used
-      const float* src = p.o_part + (static_cast<long long>(s) * p.rows + row) * HEAD_DIM + lane * VEC;
-      if constexpr (VEC == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-        acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
-      } else {
-        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
-        acc[0] += ws * v.x; acc[1] += ws * v.y;
-      }
-    }
-    const float inv = 1.0f / W;
+      for (int s = kSpec; s < n; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+        if (ws == 0.f) continue;  // empty split (or a weight that underflows): not used
+        float v[VEC];
+        detail::load_vec<VEC>(o_at(s), v);
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) acc[i] *= inv;
-    lse_out = M + 0.69314718055994531f * __log2f(W);
+        for (int i = 0; i < VEC; ++i) acc[i] += ws * v[i];
+      }
+      const float inv = 1.0f / W;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) acc[i] *= inv;
+      lse_out = M + 0.69314718055994531f * __log2f(W);
+    }
+  } else {
+    // many splits: the maximum first, then weights and sums, 32 at a time
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < n; s0 += 32)
+      if (s0 + lane < n) M = fmaxf(M, lse_at(s0 + lane));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M != -INFINITY) {
+      float W = 0.f;
+      for (int s0 = 0; s0 < n; s0 += 32) {
+        const float l = s0 + lane < n ? lse_at(s0 + lane) : -INFINITY;
+        const float w = l == -INFINITY ? 0.f : ptx::ex2_approx((l - M) * kLog2e);
+        W += w;
+        const int cnt = n - s0 < 32 ? n - s0 : 32;
+        for (int j = 0; j < cnt; ++j) {
+          const float ws = __shfl_sync(0xffffffffu, w, j);
+          if (ws == 0.f) continue;
+          float v[VEC];
+          detail::load_vec<VEC>(o_at(s0 + j), v);
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) acc[i] += ws * v[i];
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+      const float inv = 1.0f / W;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) acc[i] *= inv;
+      lse_out = M + 0.69314718055994531f * __log2f(W);
+    }
   }
 
   if (p.out_fp32) {

@@ -293,3 +293,16 @@ def test_batch_larger_than_shared_length_table(splits):
     ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, causal=True)
     out, lse = run_gpu(inp, splits, torch.bfloat16, causal=True)
     assert_close(out, lse, *ref, f"B=600 splits={splits}")
+
+
+def test_one_long_pair_more_than_64_pieces():
+    """One sequence on one KV head, 256 blocks over 152 CTAs: the balanced plan
+    cuts it into 152 pieces, more than the 64 the combine keeps in registers,
+    so the combine takes its many-splits loop."""
+    inp = _random_batch(1, 32768, 1, 4, 1, 128, seed=41, lo=32768)
+    desc = g.make_desc(inp.q, inp.k_cache)
+    C, mode, slots, items = g.gqa_decode_plan(desc, inp.seqlens.tolist(), 0, 0)
+    assert mode == 1 and max(int(r[7]) for r in items) > 64
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    out, lse = run_gpu(inp, 0, torch.float32)
+    assert_close(out, lse, *ref, "one pair, 256 blocks")

@@ -128,3 +128,12 @@ def test_auto_falls_back_to_splits_for_huge_batches():
     lens = [300] * 1500
     C, mode, slots, items = g.gqa_decode_plan(_desc(1500, 1, 300), lens, 0, 152)
     assert mode == 0
+
+
+def test_balanced_plan_can_exceed_64_pieces_per_pair():
+    """A long sequence on few KV heads is cut over every CTA: 152 pieces for
+    one pair, which the combine must merge beyond its 64-slot fast path."""
+    C, mode, slots, items = g.gqa_decode_plan(_desc(1, 1, 32768), [32768], 0, 152)
+    assert mode == 1 and slots == 152
+    assert max(int(r[7]) for r in items) == 152
+    check_balanced([32768], 1, 32768, 152)
