@@ -211,8 +211,9 @@ def bench_ours(args, cfg, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     splits = args.splits
-    out_dtype = torch.float32 if cfg.out_dtype == "fp32" else torch.bfloat16
-    host = workloads.make_inputs(cfg)
+    in_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    out_dtype = torch.float32 if cfg.out_dtype == "fp32" else in_dtype
+    host = workloads.make_inputs(cfg, dtype=in_dtype)
     kv_bytes = host.kv_bytes()
     alloc_bytes = host.k_cache.numel() * 2 * 2
     pool = max(2, math.ceil(args.pool_mb * 2**20 / alloc_bytes) + 1)
@@ -331,7 +332,8 @@ def bench_ours(args, cfg, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5), "us_per_call": round(ms_step_max * 1e3, 3),
         "frac_of_peak": round(value / world / peak, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic: seeded randn rounded to bf16",
+        "vs_baseline": None, "dtype": "f16" if args.dtype == "fp16" else "bf16",
+        "data": f"synthetic: seeded randn rounded to {args.dtype}",
         "config": {"workload": cfg.name, "description": cfg.description, "batch": cfg.batch,
                    "q_tokens": cfg.q_tokens, "q_heads": cfg.q_heads, "kv_heads": cfg.kv_heads,
                    "head_dim": cfg.head_dim, "seqlen": cfg.seqlen if cfg.ragged is None else "ragged",
@@ -370,7 +372,7 @@ def bench_reference(args, cfg):
 
     orc = oracle.load()
     cores = len(os.sched_getaffinity(0))
-    host = workloads.make_inputs(cfg)
+    host = workloads.make_inputs(cfg, dtype=torch.float16 if args.dtype == "fp16" else torch.bfloat16)
     B = cfg.batch
     per_b = [int(L) * cfg.kv_heads * cfg.head_dim * 4 for L in host.seqlens.tolist()]
 
@@ -408,6 +410,7 @@ def main(argv=None):
     ap.add_argument("--config", default="llama8b", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--splits", type=int, default=None, help="0 = automatic (default: the config's first)")
     ap.add_argument("--pool-mb", type=float, default=512.0)
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16", help="element type of q, k and v")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")

@@ -26,6 +26,7 @@ GQA_ERR_TIMEOUT = 5
 GQA_ERR_BAD_SEQLEN = 6
 GQA_DTYPE_BF16 = 0
 GQA_DTYPE_FP32 = 1
+GQA_DTYPE_FP16 = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +49,7 @@ class gqa_desc_t(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("causal", ctypes.c_int),
         ("out_dtype", ctypes.c_int),
+        ("in_dtype", ctypes.c_int),
     ]
 
 
@@ -114,8 +116,18 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _dtype_code(dtype, allowed):
+    import torch
+
+    code = {torch.bfloat16: GQA_DTYPE_BF16, torch.float32: GQA_DTYPE_FP32, torch.float16: GQA_DTYPE_FP16}.get(dtype)
+    if code is None or code not in allowed:
+        raise ValueError(f"unsupported dtype {dtype}")
+    return code
+
+
 def make_desc(q, k_cache, *, scale: float = 0.0, causal: bool = False, out_dtype=None) -> gqa_desc_t:
-    """Problem description from q [B, nq, Hq, d] and a cache [B, S_max, Hkv, d]."""
+    """Problem description from q [B, nq, Hq, d] and a cache [B, S_max, Hkv, d]
+    (inputs bf16 or fp16; out_dtype fp32 or the inputs' type, the default)."""
     import torch
 
     B, nq, Hq, d = q.shape
@@ -123,19 +135,18 @@ def make_desc(q, k_cache, *, scale: float = 0.0, causal: bool = False, out_dtype
     if Bk != B or dk != d:
         raise ValueError(f"q {tuple(q.shape)} and cache {tuple(k_cache.shape)} disagree")
     if out_dtype is None:
-        out_dtype = torch.bfloat16
-    code = {torch.bfloat16: GQA_DTYPE_BF16, torch.float32: GQA_DTYPE_FP32}.get(out_dtype)
-    if code is None:
-        raise ValueError(f"unsupported output dtype {out_dtype}")
-    return gqa_desc_t(B, nq, Hq, Hkv, d, s_max, float(scale), int(bool(causal)), code)
+        out_dtype = q.dtype
+    code = _dtype_code(out_dtype, (GQA_DTYPE_BF16, GQA_DTYPE_FP32, GQA_DTYPE_FP16))
+    in_code = _dtype_code(q.dtype, (GQA_DTYPE_BF16, GQA_DTYPE_FP16))
+    return gqa_desc_t(B, nq, Hq, Hkv, d, s_max, float(scale), int(bool(causal)), code, in_code)
 
 
 def _inputs_ok(q, k_cache, v_cache, seqlens):
     import torch
 
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
-        if t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 tensor")
+        if t.dtype not in (torch.bfloat16, torch.float16) or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 or fp16 tensor, all three of one type")
     if v_cache.shape != k_cache.shape:
         raise ValueError("k_cache and v_cache shapes differ")
     if seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
@@ -208,7 +219,7 @@ def gqa_decode_combine(o_part, lse_part, out, lse=None, stream=None) -> None:
 
     S, d = o_part.shape[0], o_part.shape[-1]
     rows = lse_part[0].numel()
-    code = {torch.bfloat16: GQA_DTYPE_BF16, torch.float32: GQA_DTYPE_FP32}[out.dtype]
+    code = _dtype_code(out.dtype, (GQA_DTYPE_BF16, GQA_DTYPE_FP32, GQA_DTYPE_FP16))
     rc = lib().gqa_decode_combine(_ptr(o_part), _ptr(lse_part), int(S), int(rows), int(d), _ptr(out), code,
                                   _ptr(lse), _stream(stream))
     _check(rc, "gqa_decode_combine")
@@ -253,7 +264,7 @@ def decode(q, k_cache, v_cache, seqlens, *, num_splits: int = 0, scale: float = 
     """Allocates out / lse / workspace with torch and calls gqa_decode_attn."""
     import torch
 
-    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    out_dtype = q.dtype if out_dtype is None else out_dtype
     B, nq, Hq, d = q.shape
     out = torch.empty(B, nq, Hq, d, dtype=out_dtype, device=q.device)
     lse = torch.empty(B, nq, Hq, dtype=torch.float32, device=q.device)

@@ -17,6 +17,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sm103_ptx.cuh"
 
@@ -28,11 +29,11 @@ struct CombineParams {
   const float* o_part;      // [num_splits, rows, d]
   const float* lse_part;    // [num_splits, rows]
   const int32_t* n_pieces;  // optional [B * Hkv][4]: valid slots per pair in [0] (balanced plan)
-  void* out;                // [rows, d] bf16 or fp32
+  void* out;                // [rows, d] bf16, fp16 or fp32
   float* lse;               // [rows] or null
   long long rows;
   int num_splits;           // slots per row (all of them are merged when n_pieces is null)
-  int out_fp32;
+  int out_dtype;            // 0 bf16, 1 fp32, 2 fp16 (gqa_dtype_t)
   int nq, Hq, G, kv_heads;  // row -> pair mapping for n_pieces
 };
 
@@ -177,22 +178,26 @@ gqa_combine_kernel(const CombineParams p) {
     }
   }
 
-  if (p.out_fp32) {
+  if (p.out_dtype == 1) {  // fp32
     float* dst = static_cast<float*>(p.out) + row * HEAD_DIM + lane * VEC;
     if constexpr (VEC == 4) *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     else *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
   } else {
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + row * HEAD_DIM + lane * VEC;
-    if constexpr (VEC == 4) {
-      __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
-      __nv_bfloat162 c = __floats2bfloat162_rn(acc[2], acc[3]);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&a);
-      u.y = *reinterpret_cast<uint32_t*>(&c);
-      *reinterpret_cast<uint2*>(dst) = u;
-    } else {
-      *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0], acc[1]);
+    // two 16-bit values per 32-bit word, bf16 or fp16
+    uint32_t w[VEC / 2];
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i) {
+      if (p.out_dtype == 2) {
+        __half2 h = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+      } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+      }
     }
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + row * HEAD_DIM + lane * VEC;
+    if constexpr (VEC == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    else *reinterpret_cast<uint32_t*>(dst) = w[0];
   }
   if (lane == 0 && p.lse != nullptr) p.lse[row] = lse_out;
   ptx::griddep_launch_dependents();

@@ -52,6 +52,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "plan.cuh"
 #include "sm103_ptx.cuh"
@@ -91,6 +92,9 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 #define GQA_TRACE_EVENT(ev, idx) ((void)(idx))  // index evaluated in both builds
 #endif
 
+// output element types (the values of gqa_dtype_t)
+constexpr int kOutBF16 = 0, kOutF32 = 1, kOutF16 = 2;
+
 constexpr int kThreads = 224;       // producer, QK issuer, PV issuer, 4 softmax warps
 constexpr int kSoftmaxThread0 = 96;  // first thread of the softmax warpgroup
 constexpr int kMaxSmemB = 512;       // sequences whose lengths are staged in shared memory
@@ -100,18 +104,18 @@ constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kSCol0 = 0, kSCol1 = 32, kOCol = 64;
 
 struct DecodeParams {
-  CUtensorMap tm_q;  // q [B, nq, Hq, d] bf16, box {64, G, nq, 1}
-  CUtensorMap tm_k;  // k_cache [B, S_max, Hkv, d] bf16, box {64, 1, 128, 1}
+  CUtensorMap tm_q;  // q [B, nq, Hq, d] bf16 or fp16, box {64, G, nq, 1}
+  CUtensorMap tm_k;  // k_cache [B, S_max, Hkv, d] bf16 or fp16, box {64, 1, 128, 1}
   CUtensorMap tm_v;  // v_cache, same
   const int32_t* seqlens;
-  void* out;          // [B, nq, Hq, d] bf16 or fp32
+  void* out;          // [B, nq, Hq, d] bf16, fp16 or fp32
   float* lse;         // [B, nq, Hq] or null
   float* o_part;      // [slots, B*nq*Hq, d]
   float* lse_part;    // [slots, B*nq*Hq]
   int32_t* n_pieces;  // [B*Hkv] (PLAN_BALANCED)
   PlanParams plan;
   int nq, Hq, G, head_dim;
-  int out_fp32;
+  int out_dtype;      // 0 bf16, 1 fp32, 2 fp16 (gqa_dtype_t); 16-bit outputs have the input type
   int causal;
   float scale_log2;   // softmax scale * log2(e)
   int lse_bulk;       // LSE rows may be written by 16-byte bulk copies (G % 4 == 0, aligned)
@@ -227,7 +231,8 @@ struct ItemSource {
   }
 };
 
-template <int HEAD_DIM, int NPAD>
+// IN_F16: q, k, v (and P) are fp16; otherwise bf16.
+template <int HEAD_DIM, int NPAD, bool IN_F16>
 __global__ void __launch_bounds__(kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HEAD_DIM, NPAD>;
@@ -435,7 +440,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     const long long pair_idx = static_cast<long long>(wi.b) * plan.kv_heads + wi.h;
     const bool with_o = wi.blk_begin < wi.blk_end;  // an empty split publishes only lse = -inf
     const bool final_out = wi.slot < 0;
-    const uint32_t esz = (final_out && !p.out_fp32) ? 2u : 4u;
+    const uint32_t esz = (final_out && p.out_dtype != kOutF32) ? 2u : 4u;
     const uint32_t row_bytes = static_cast<uint32_t>(p.G) * HEAD_DIM * esz;
     const float* lse_st = lse_of(ob);
     for (int t = 0; t < p.nq; ++t) {
@@ -560,7 +565,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       iter.init(list_hdr, list_items, plan, lens_raw, s_len, s_pre);
       WorkItem it;
       if (is_qk) {
-        constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, NPAD, 0, 0);
+        constexpr uint32_t idesc_qk = ptx::idesc_f16_f32(128, NPAD, 0, 0, !IN_F16);
         while (ok && iter.next(it)) {
           if (it.blk_begin >= it.blk_end) continue;
           const int qb = kq & 1;
@@ -583,7 +588,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
             for (int k = 0; k < HEAD_DIM / 16; ++k) {
               const uint32_t off_a = static_cast<uint32_t>((k >> 2) * (16384 >> 4) + (k & 3) * 2);
               const uint32_t off_b = static_cast<uint32_t>((k >> 2) * (NPAD * 128 >> 4) + (k & 3) * 2);
-              ptx::mma_bf16_ss(d_tmem, kd + off_a, qd + off_b, idesc_qk, k > 0 ? 1u : 0u);
+              ptx::mma_f16_ss(d_tmem, kd + off_a, qd + off_b, idesc_qk, k > 0 ? 1u : 0u);
             }
             ptx::mma_commit(BAR(S_FULL + sl));
             ptx::mma_commit(BAR(RING_EMPTY + stage));
@@ -593,7 +598,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           ++kq;
         }
       } else {
-        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, Cfg::kOWidth, 1, 0);
+        constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, Cfg::kOWidth, 1, 0, !IN_F16);
         uint32_t k = 0;  // items
         while (ok && iter.next(it)) {
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
@@ -617,13 +622,13 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
                 const uint32_t off_b = static_cast<uint32_t>((k >> 2) * (NPAD * 128 >> 4) + (k & 3) * 2);
-                ptx::mma_bf16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)), pd + off_b,
+                ptx::mma_f16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)), pd + off_b,
                                  idesc_pv, (k > 0 || !first) ? 1u : 0u);
               }
             } else {
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                ptx::mma_bf16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)),
+                ptx::mma_f16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)),
                                  pd + static_cast<uint32_t>(k * 2), idesc_pv, (k > 0 || !first) ? 1u : 0u);
               }
             }
@@ -747,8 +752,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         uint8_t* ob = obuf_of(static_cast<int>(k_out & 1u));
         if (r < HEAD_DIM) {
           for (int n = 0; n < nv; ++n) {
-            if (it.slot < 0 && !p.out_fp32)
-              reinterpret_cast<__nv_bfloat16*>(ob)[n * HEAD_DIM + r] = __float2bfloat16_rn(0.f);
+            if (it.slot < 0 && p.out_dtype != kOutF32)
+              reinterpret_cast<__nv_bfloat16*>(ob)[n * HEAD_DIM + r] = __float2bfloat16_rn(0.f);  // +0: all-zero bits
             else
               reinterpret_cast<float*>(ob)[n * HEAD_DIM + r] = 0.f;
           }
@@ -867,7 +872,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
           for (int n = 0; n < NPAD; ++n) {
             const int sw = chunk ^ (n & 7);
-            *reinterpret_cast<__nv_bfloat16*>(pb + n * 128 + sw * 16 + within) = __float2bfloat16_rn(pr[n]);
+            if constexpr (IN_F16)
+              *reinterpret_cast<__half*>(pb + n * 128 + sw * 16 + within) = __float2half_rn(pr[n]);
+            else
+              *reinterpret_cast<__nv_bfloat16*>(pb + n * 128 + sw * 16 + within) = __float2bfloat16_rn(pr[n]);
           }
           // Tail block: V rows past the sequence end hold whatever the cache
           // holds there; zero them so that 0 * garbage cannot poison O.
@@ -942,15 +950,23 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       // Outputs go to shared memory in their global layout (row n = t*G + g
       // of this pair, d contiguous); the output warp writes them out.
       if (writer) {
-        const bool as_bf16 = it.slot < 0 && !p.out_fp32;
+        // fp32 for partials and fp32 outputs, else 16-bit outputs of the
+        // input type
+        const bool out16 = it.slot < 0 && p.out_dtype != kOutF32;
         uint8_t* obuf = obuf_of(static_cast<int>(k_out & 1u));
 #pragma unroll
         for (int n = 0; n < NPAD; ++n) {
           const float inv = lt[n] > 0.f ? ptx::rcp_approx(lt[n]) : 0.f;
           const float val = o[n] * inv;
           if (n < nv) {
-            if (as_bf16) reinterpret_cast<__nv_bfloat16*>(obuf)[n * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
-            else reinterpret_cast<float*>(obuf)[n * HEAD_DIM + d_row] = val;
+            if (out16) {
+              if constexpr (IN_F16)
+                reinterpret_cast<__half*>(obuf)[n * HEAD_DIM + d_row] = __float2half_rn(val);
+              else
+                reinterpret_cast<__nv_bfloat16*>(obuf)[n * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
+            } else {
+              reinterpret_cast<float*>(obuf)[n * HEAD_DIM + d_row] = val;
+            }
           }
         }
         if (d_row < nv) {

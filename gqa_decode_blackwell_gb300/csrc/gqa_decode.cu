@@ -92,7 +92,11 @@ gqa_status_t check_desc(const gqa_desc_t* d) {
   if (d->batch < 0 || d->q_tokens < 1 || d->q_heads < 1 || d->kv_heads < 1 || d->max_seqlen < 1)
     return GQA_ERR_INVALID_ARG;
   if (d->q_heads % d->kv_heads != 0) return GQA_ERR_INVALID_ARG;
-  if (d->out_dtype != GQA_DTYPE_BF16 && d->out_dtype != GQA_DTYPE_FP32) return GQA_ERR_INVALID_ARG;
+  if (d->out_dtype != GQA_DTYPE_BF16 && d->out_dtype != GQA_DTYPE_FP32 && d->out_dtype != GQA_DTYPE_FP16)
+    return GQA_ERR_INVALID_ARG;
+  if (d->in_dtype != GQA_DTYPE_BF16 && d->in_dtype != GQA_DTYPE_FP16) return GQA_ERR_INVALID_ARG;
+  // a 16-bit output has the inputs' type (fp32 goes with either)
+  if (d->out_dtype != GQA_DTYPE_FP32 && d->out_dtype != d->in_dtype) return GQA_ERR_UNSUPPORTED;
   if (!(d->scale >= 0.f) || std::isinf(d->scale)) return GQA_ERR_INVALID_ARG;
   if (d->head_dim != 64 && d->head_dim != 128) return GQA_ERR_UNSUPPORTED;
   const long long g = d->q_heads / d->kv_heads;
@@ -184,12 +188,14 @@ gqa_status_t encode_maps(const gqa_desc_t* d, const void* q, const void* k, cons
   const cuuint64_t D = static_cast<cuuint64_t>(d->head_dim);
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const int G = d->q_heads / d->kv_heads;
+  const CUtensorMapDataType in_type =
+      d->in_dtype == GQA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   {
     const cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(d->q_heads), static_cast<cuuint64_t>(d->q_tokens),
                                 static_cast<cuuint64_t>(d->batch)};
     const cuuint64_t strides[3] = {D * 2, D * 2 * d->q_heads, D * 2 * d->q_heads * d->q_tokens};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(d->q_tokens), 1};
-    if (enc(&p->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, es,
+    if (enc(&p->tm_q, in_type, 4, const_cast<void*>(q), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return GQA_ERR_INVALID_ARG;
@@ -201,7 +207,7 @@ gqa_status_t encode_maps(const gqa_desc_t* d, const void* q, const void* k, cons
   CUtensorMap* maps[2] = {&p->tm_k, &p->tm_v};
   const void* ptrs[2] = {k, v};
   for (int i = 0; i < 2; ++i) {
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptrs[i]), dims, strides, box, es,
+    if (enc(maps[i], in_type, 4, const_cast<void*>(ptrs[i]), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return GQA_ERR_INVALID_ARG;
@@ -217,10 +223,10 @@ cudaLaunchAttribute pdl_attr(bool on) {
   return a;
 }
 
-template <int HD, int NP>
+template <int HD, int NP, bool F16>
 gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodeParams& p, cudaStream_t s) {
   using Cfg = DecodeCfg<HD, NP>;
-  const void* fn = reinterpret_cast<const void*>(&gqa_decode_kernel<HD, NP>);
+  const void* fn = reinterpret_cast<const void*>(&gqa_decode_kernel<HD, NP, F16>);
   gqa_status_t rc = ensure_smem_attr(st, attr_bit, fn, Cfg::kSmemBytes);
   if (rc != GQA_OK) return rc;
   cudaLaunchConfig_t cfg;
@@ -232,16 +238,22 @@ gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodePar
   cudaLaunchAttribute attr = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HD, NP>, p) != cudaSuccess) return GQA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HD, NP, F16>, p) != cudaSuccess) return GQA_ERR_CUDA;
   return GQA_OK;
 }
 
-gqa_status_t launch_decode(DeviceState* st, const DecodeParams& p, cudaStream_t s) {
+template <bool F16>
+gqa_status_t launch_decode_dt(DeviceState* st, const DecodeParams& p, cudaStream_t s) {
   const int nv = p.nq * p.G;
+  const unsigned b = F16 ? 4u : 0u;
   if (p.head_dim == 64) {
-    return nv <= 16 ? launch_decode_t<64, 16>(st, 0, p, s) : launch_decode_t<64, 32>(st, 1, p, s);
+    return nv <= 16 ? launch_decode_t<64, 16, F16>(st, b + 0, p, s) : launch_decode_t<64, 32, F16>(st, b + 1, p, s);
   }
-  return nv <= 16 ? launch_decode_t<128, 16>(st, 2, p, s) : launch_decode_t<128, 32>(st, 3, p, s);
+  return nv <= 16 ? launch_decode_t<128, 16, F16>(st, b + 2, p, s) : launch_decode_t<128, 32, F16>(st, b + 3, p, s);
+}
+
+gqa_status_t launch_decode(DeviceState* st, const DecodeParams& p, bool in_f16, cudaStream_t s) {
+  return in_f16 ? launch_decode_dt<true>(st, p, s) : launch_decode_dt<false>(st, p, s);
 }
 
 gqa_status_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t s) {
@@ -280,7 +292,7 @@ gqa_status_t prepare_decode(const gqa_desc_t* d, const void* q, const void* k, c
   p->Hq = d->q_heads;
   p->G = d->q_heads / d->kv_heads;
   p->head_dim = d->head_dim;
-  p->out_fp32 = d->out_dtype == GQA_DTYPE_FP32;
+  p->out_dtype = d->out_dtype;
   p->causal = d->causal != 0;
   const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
   p->scale_log2 = scale * 1.4426950408889634f;
@@ -353,7 +365,7 @@ gqa_status_t attn_impl(const gqa_desc_t* desc, const void* q, const void* k_cach
     p.o_part = o_part;
     p.lse_part = lse_part;
     p.n_pieces = n_pieces;
-    if ((rc = launch_decode(st, p, s)) != GQA_OK) return rc;
+    if ((rc = launch_decode(st, p, desc->in_dtype == GQA_DTYPE_FP16, s)) != GQA_OK) return rc;
   }
   if (!(parts & ATTN_MERGE) || !hp.combine) return GQA_OK;
   CombineParams c;
@@ -365,7 +377,7 @@ gqa_status_t attn_impl(const gqa_desc_t* desc, const void* q, const void* k_cach
   c.lse = lse;
   c.rows = static_cast<long long>(desc->batch) * desc->q_tokens * desc->q_heads;
   c.num_splits = hp.num_slots;
-  c.out_fp32 = desc->out_dtype == GQA_DTYPE_FP32;
+  c.out_dtype = desc->out_dtype;
   c.nq = desc->q_tokens;
   c.Hq = desc->q_heads;
   c.G = desc->q_heads / desc->kv_heads;
@@ -466,14 +478,15 @@ gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const voi
   if ((rc = prepare_decode(desc, q, k_cache, v_cache, seqlens, hp, &p)) != GQA_OK) return rc;
   p.o_part = o_part;
   p.lse_part = lse_part;
-  return launch_decode(st, p, static_cast<cudaStream_t>(stream));
+  return launch_decode(st, p, desc->in_dtype == GQA_DTYPE_FP16, static_cast<cudaStream_t>(stream));
 }
 
 gqa_status_t gqa_decode_combine(const float* o_part, const float* lse_part, int num_splits, int64_t rows,
                                 int head_dim, void* out, int out_dtype, float* lse, void* stream) {
   if (num_splits < 1 || num_splits > GQA_MAX_SPLITS || rows < 0) return GQA_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return GQA_ERR_UNSUPPORTED;
-  if (out_dtype != GQA_DTYPE_BF16 && out_dtype != GQA_DTYPE_FP32) return GQA_ERR_INVALID_ARG;
+  if (out_dtype != GQA_DTYPE_BF16 && out_dtype != GQA_DTYPE_FP32 && out_dtype != GQA_DTYPE_FP16)
+    return GQA_ERR_INVALID_ARG;
   if (rows == 0) return GQA_OK;
   if (o_part == nullptr || lse_part == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
   if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(out, 16) || (lse != nullptr && !aligned(lse, 4)))
@@ -486,7 +499,7 @@ gqa_status_t gqa_decode_combine(const float* o_part, const float* lse_part, int 
   c.lse = lse;
   c.rows = rows;
   c.num_splits = num_splits;
-  c.out_fp32 = out_dtype == GQA_DTYPE_FP32;
+  c.out_dtype = out_dtype;
   c.nq = c.Hq = c.G = c.kv_heads = 1;
   return launch_combine(c, head_dim, static_cast<cudaStream_t>(stream));
 }

@@ -83,7 +83,8 @@ class DecodeInputs:
         return int(self.k_cache.shape[1])
 
     def kv_bytes(self) -> int:
-        """Bytes of K and V a decode must read: 4*d bytes per position per KV head."""
+        """Bytes of K and V a decode must read: 4*d bytes per position per KV head
+        (2-byte elements, bf16 or fp16)."""
         c = self.config
         return int(self.seqlens.clamp(min=0).sum().item()) * c.kv_heads * c.head_dim * 2 * 2
 
@@ -99,24 +100,28 @@ def seqlens_for(cfg: DecodeConfig, gen: torch.Generator) -> torch.Tensor:
     return torch.full((cfg.batch,), cfg.seqlen, dtype=torch.int32)
 
 
-def make_inputs(cfg: DecodeConfig, seed: Optional[int] = None, capacity: Optional[int] = None) -> DecodeInputs:
-    """Seeded CPU inputs for a config (see the module docstring for the recipe)."""
+def make_inputs(cfg: DecodeConfig, seed: Optional[int] = None, capacity: Optional[int] = None,
+                dtype: torch.dtype = torch.bfloat16) -> DecodeInputs:
+    """Seeded CPU inputs for a config (see the module docstring for the recipe);
+    dtype: the element type q, k and v are rounded to (bf16 or fp16)."""
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"inputs are bf16 or fp16, not {dtype}")
     gen = torch.Generator().manual_seed(cfg.seed if seed is None else seed)
     seqlens = seqlens_for(cfg, gen)
     s_max = int(seqlens.max().item()) if cfg.batch > 0 else 0
     if capacity is not None:
         s_max = max(s_max, int(capacity))
     B, nq, Hq, Hkv, d = cfg.batch, cfg.q_tokens, cfg.q_heads, cfg.kv_heads, cfg.head_dim
-    q = torch.randn(B, nq, Hq, d, generator=gen).to(torch.bfloat16)
+    q = torch.randn(B, nq, Hq, d, generator=gen).to(dtype)
     k32 = [torch.randn(s_max, Hkv, d, generator=gen) for _ in range(B)]
-    v = torch.stack([torch.randn(s_max, Hkv, d, generator=gen).to(torch.bfloat16) for _ in range(B)]) \
-        if B > 0 else torch.empty(0, s_max, Hkv, d, dtype=torch.bfloat16)
+    v = torch.stack([torch.randn(s_max, Hkv, d, generator=gen).to(dtype) for _ in range(B)]) \
+        if B > 0 else torch.empty(0, s_max, Hkv, d, dtype=dtype)
     extras = {}
     if cfg.key_offset_std > 0:
         off = torch.randn(Hkv, generator=gen) * cfg.key_offset_std
         extras["key_offset"] = off
         k32 = [kb + off.view(1, Hkv, 1) for kb in k32]
-    k = torch.stack([kb.to(torch.bfloat16) for kb in k32]) if B > 0 else torch.empty_like(v)
+    k = torch.stack([kb.to(dtype) for kb in k32]) if B > 0 else torch.empty_like(v)
     return DecodeInputs(cfg, q, k, v, seqlens, 1.0 / float(d) ** 0.5, extras)
 
 

@@ -54,10 +54,12 @@ typedef enum {
   GQA_ERR_BAD_SEQLEN = 6    /* a sequence length was < 0 or > max_seqlen */
 } gqa_status_t;
 
-typedef enum { GQA_DTYPE_BF16 = 0, GQA_DTYPE_FP32 = 1 } gqa_dtype_t;
+typedef enum { GQA_DTYPE_BF16 = 0, GQA_DTYPE_FP32 = 1, GQA_DTYPE_FP16 = 2 } gqa_dtype_t;
 
-/* Problem description.  Q is bf16 [batch, q_tokens, q_heads, head_dim];
- * the K and V caches are bf16 [batch, max_seqlen, kv_heads, head_dim]. */
+/* Problem description.  Q is [batch, q_tokens, q_heads, head_dim]; the K
+ * and V caches are [batch, max_seqlen, kv_heads, head_dim]; all three are
+ * in_dtype (bf16 or fp16).  Scores, softmax and accumulation are fp32; P
+ * enters the value MMA in in_dtype. */
 typedef struct {
   int batch;       /* B >= 0 */
   int q_tokens;    /* nq >= 1 new query tokens per sequence */
@@ -67,7 +69,9 @@ typedef struct {
   int max_seqlen;  /* S_max >= 1: cache capacity along positions */
   float scale;     /* softmax scale; 0 selects 1/sqrt(head_dim) */
   int causal;      /* nonzero: causal mask among the nq new tokens */
-  int out_dtype;   /* gqa_dtype_t of `out` */
+  int out_dtype;   /* gqa_dtype_t of `out`: FP32, or in_dtype (a 16-bit
+                      output of the other 16-bit type is GQA_ERR_UNSUPPORTED) */
+  int in_dtype;    /* gqa_dtype_t of q, k_cache, v_cache: BF16 or FP16 */
 } gqa_desc_t;
 
 /* Limits: q_tokens * (q_heads / kv_heads) <= 32 query rows per KV head, and
@@ -91,9 +95,9 @@ size_t gqa_decode_workspace_size(const gqa_desc_t* desc, int num_splits);
  * log-sum-exp combine kernel, chained with programmatic dependent launch
  * ("Building a Faster GQA Decode Kernel for Blackwell SM100", section
  * "Starting combine early with PDL").
- *   q          bf16 [B, nq, Hq, d], 16-byte aligned
- *   k_cache    bf16 [B, S_max, Hkv, d], 16-byte aligned
- *   v_cache    bf16 [B, S_max, Hkv, d], 16-byte aligned
+ *   q          in_dtype [B, nq, Hq, d], 16-byte aligned
+ *   k_cache    in_dtype [B, S_max, Hkv, d], 16-byte aligned
+ *   v_cache    in_dtype [B, S_max, Hkv, d], 16-byte aligned
  *   seqlens    int32 [B] device array; L_b in [0, S_max] (values outside are
  *              clamped and flagged as GQA_ERR_BAD_SEQLEN by
  *              gqa_decode_get_error).  Positions in [L_b, S_max) may hold any

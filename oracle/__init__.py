@@ -35,6 +35,7 @@ class _Shape(ctypes.Structure):
         ("max_seqlen", ctypes.c_int),
         ("scale", ctypes.c_double),
         ("causal", ctypes.c_int),
+        ("in_fp16", ctypes.c_int),
     ]
 
 
@@ -47,14 +48,20 @@ def build(out_path: str = _LIB, mutant: int = 0) -> str:
 
 
 def _np_u16(t):
-    """Raw bf16 bit patterns of a CPU tensor / array, as a contiguous uint16 array."""
+    """Raw bf16 / fp16 bit patterns of a CPU tensor / array, as a contiguous uint16 array."""
     if isinstance(t, np.ndarray):
         assert t.dtype == np.uint16
         return np.ascontiguousarray(t)
     import torch
 
-    assert t.dtype == torch.bfloat16, "the oracle takes the exact bf16 inputs"
+    assert t.dtype in (torch.bfloat16, torch.float16), "the oracle takes the exact bf16 or fp16 inputs"
     return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _is_fp16(t):
+    import torch
+
+    return (not isinstance(t, np.ndarray)) and t.dtype == torch.float16
 
 
 def _ptr(a, ctype):
@@ -78,24 +85,33 @@ class Oracle:
             ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
             ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
         ]
+        lib.gqa_oracle_elem.restype = ctypes.c_double
+        lib.gqa_oracle_elem.argtypes = [ctypes.c_int, ctypes.c_uint16]
         self._lib = lib
         self.path = path
+
+    def elem(self, bits: int, fp16: bool) -> float:
+        """The value the oracle reads for one 16-bit input pattern."""
+        return float(self._lib.gqa_oracle_elem(int(bool(fp16)), int(bits)))
 
     def decode(self, q, k, v, seqlens, *, scale=None, causal=False, pos_begin=None, pos_end=None,
                nthreads=None):
         """Exact attention per (b, t, hq) row.
 
-        q: bf16 [B, nq, Hq, d]; k, v: bf16 [B, S_max, Hkv, d]; seqlens: int [B].
+        q: bf16 or fp16 [B, nq, Hq, d]; k, v: the same type, [B, S_max, Hkv, d];
+        seqlens: int [B].
         pos_begin / pos_end: optional int [B] bounds on key positions (a split).
         Returns (out float64 [B, nq, Hq, d], lse float64 [B, nq, Hq]).
         """
+        in_fp16 = _is_fp16(q)
+        assert _is_fp16(k) == in_fp16 and _is_fp16(v) == in_fp16, "q, k and v share one element type"
         qa, ka, va = _np_u16(q), _np_u16(k), _np_u16(v)
         B, nq, Hq, d = qa.shape
         Bk, S_max, Hkv, dk = ka.shape
         assert va.shape == ka.shape and Bk == B and dk == d
         sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32).reshape(B))
         sh = _Shape(B, nq, Hq, Hkv, d, S_max, float(1.0 / np.sqrt(d) if scale is None else scale),
-                    int(bool(causal)))
+                    int(bool(causal)), int(in_fp16))
         pb = None if pos_begin is None else np.ascontiguousarray(np.asarray(pos_begin, dtype=np.int32).reshape(B))
         pe = None if pos_end is None else np.ascontiguousarray(np.asarray(pos_end, dtype=np.int32).reshape(B))
         out = np.empty((B, nq, Hq, d), dtype=np.float64)

@@ -31,7 +31,10 @@
  *    splits, weights w_s = exp(lse_s - M) and returns
  *    O = sum_s w_s O_s / sum_s w_s, lse = M + ln(sum_s w_s).
  *
- * Inputs are the exact bf16 values (raw 16-bit patterns), widened to double.
+ * Inputs are the exact bf16 or fp16 values (raw 16-bit patterns), widened to
+ * double: bf16 is the upper half of an IEEE binary32; fp16 is IEEE binary16
+ * (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits; exponent 0
+ * holds zero and the subnormals fraction * 2^-24, exponent 31 inf and NaN).
  *
  * Compile with -DORACLE_MUTANT=<n> to plant one deliberate mistake; the test
  * suite builds each mutant and checks that some pin rejects it.
@@ -55,6 +58,7 @@ typedef struct {
   int max_seqlen; /* S_max: cache capacity along positions */
   double scale;   /* score scale, normally 1/sqrt(d) */
   int causal;     /* bottom-right causal mask among the nq new tokens */
+  int in_fp16;    /* inputs are fp16 bit patterns (else bf16) */
 } gqa_oracle_shape;
 
 static double bf16_to_double(uint16_t h) {
@@ -62,6 +66,28 @@ static double bf16_to_double(uint16_t h) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+static double fp16_to_double(uint16_t h) {
+  const int sign = h >> 15, e = (h >> 10) & 0x1f, frac = h & 0x3ff;
+  double mag;
+  if (e == 0) {
+    mag = ldexp((double)frac, -24); /* zero and subnormals */
+  } else if (e == 31) {
+    mag = frac == 0 ? INFINITY : NAN;
+  } else {
+#if ORACLE_MUTANT == 14 /* mistake: exponent bias 14 instead of 15 */
+    mag = ldexp(1.0 + frac / 1024.0, e - 14);
+#else
+    mag = ldexp(1.0 + frac / 1024.0, e - 15);
+#endif
+  }
+  return sign ? -mag : mag;
+}
+
+/* One input element, widened to double. */
+double gqa_oracle_elem(int in_fp16, uint16_t bits) {
+  return in_fp16 ? fp16_to_double(bits) : bf16_to_double(bits);
 }
 
 typedef struct {
@@ -132,12 +158,12 @@ static void* oracle_rows(void* arg) {
       continue;
     }
     const uint16_t* qp = job->q + (size_t)row * d; /* q is [B, nq, Hq, d] */
-    for (int x = 0; x < d; ++x) qrow[x] = bf16_to_double(qp[x]);
+    for (int x = 0; x < d; ++x) qrow[x] = gqa_oracle_elem(sh->in_fp16, qp[x]);
     /* pass 1: scores and their max */
     double M = -INFINITY;
     for (int j = lo; j < hi; ++j) {
       double dot = 0.0;
-      for (int x = 0; x < d; ++x) dot += qrow[x] * bf16_to_double(job->k[cache_index(sh, b, j, h, x)]);
+      for (int x = 0; x < d; ++x) dot += qrow[x] * gqa_oracle_elem(sh->in_fp16, job->k[cache_index(sh, b, j, h, x)]);
 #if ORACLE_MUTANT == 1 /* mistake: scale dropped */
       s[j] = dot;
 #else
@@ -160,7 +186,7 @@ static void* oracle_rows(void* arg) {
 #else
       const uint16_t* vsrc = job->v;
 #endif
-      for (int x = 0; x < d; ++x) acc[x] += w * bf16_to_double(vsrc[cache_index(sh, b, j, h, x)]);
+      for (int x = 0; x < d; ++x) acc[x] += w * gqa_oracle_elem(sh->in_fp16, vsrc[cache_index(sh, b, j, h, x)]);
     }
 #if ORACLE_MUTANT == 7 /* mistake: no normalisation */
     for (int x = 0; x < d; ++x) o[x] = acc[x];
@@ -182,7 +208,7 @@ static void* oracle_rows(void* arg) {
 /*
  * Attention of every (b, t, hq) row over its visible keys, optionally
  * restricted to key positions [pos_begin[b], pos_end[b]) (NULL = no bound).
- * q: bf16 bits [B, nq, Hq, d]; k, v: bf16 bits [B, S_max, Hkv, d];
+ * q: bf16 or fp16 bits [B, nq, Hq, d]; k, v: the same type, [B, S_max, Hkv, d];
  * seqlens: [B] (L_b includes the nq new positions).
  * out: [B, nq, Hq, d] doubles; lse: [B, nq, Hq] doubles (natural log).
  * Returns 0, or -1 on a bad shape / allocation failure.

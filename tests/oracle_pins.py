@@ -97,6 +97,31 @@ def pin_sdpa(orc, causal=False, shape=(2, 1, 8, 2, 16, 37), seqlens=None, seed=1
     assert err < 1e-10, f"oracle vs SDPA fp64: max abs err {err}"
 
 
+def pin_fp16_widening(orc):
+    """Every one of the 65536 fp16 bit patterns widens to numpy's float16 value
+    (an independent IEEE binary16 implementation); NaN patterns stay NaN."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.elem(int(x), True) for x in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def pin_sdpa_fp16(orc):
+    """fp16 inputs against SDPA in fp64 on the same fp16 values."""
+    gen = torch.Generator().manual_seed(21)
+    B, nq, Hq, Hkv, d, S_max = 2, 2, 8, 2, 16, 31
+    q = torch.randn(B, nq, Hq, d, generator=gen).to(torch.float16)
+    k = (torch.randn(B, S_max, Hkv, d, generator=gen) * 3).to(torch.float16)
+    v = torch.randn(B, S_max, Hkv, d, generator=gen).to(torch.float16)
+    seqlens = [31, 20]
+    out, _ = orc.decode(q, k, v, seqlens, causal=True, nthreads=4)
+    ref = _sdpa_reference(q, k, v, seqlens, True)
+    err = float(np.abs(out - ref).max())
+    assert err < 1e-10, f"fp16 oracle vs SDPA fp64: max abs err {err}"
+
+
 def pin_sdpa_all(orc):
     pin_sdpa(orc, causal=False)
     pin_sdpa(orc, causal=True, shape=(3, 4, 8, 2, 16, 29), seqlens=[29, 17, 4])
@@ -294,6 +319,8 @@ def pin_combine_closed_forms(orc):
 ALL_PINS = [
     pin_bruteforce_tiny,
     pin_sdpa_all,
+    pin_fp16_widening,
+    pin_sdpa_fp16,
     pin_identical_keys,
     pin_causal_counts,
     pin_dominant_score,

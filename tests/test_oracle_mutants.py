@@ -5,7 +5,7 @@ The mutants are compiled from ``oracle/gqa_oracle.c`` with
 alignment or an off-by-one, a dropped max term, no max subtraction, values
 read from the key cache, no normalisation, one key past the end, a sign error
 or a missing max in the merge, a missing empty-row case, a transposed cache
-layout).  CPU only.
+layout, a wrong fp16 exponent bias).  CPU only.
 """
 import math
 import warnings
@@ -30,6 +30,7 @@ MUTANTS = {
     11: "cache read as [B, Hkv, S, d]",
     12: "max term dropped from merged lse",
     13: "causal limit off by one",
+    14: "fp16 exponent bias 14",
 }
 
 

@@ -78,12 +78,12 @@ def test_config_full_size(name, splits):
     assert_close(out, lse, ref_out, ref_lse, f"{name} splits={splits}")
 
 
-def _nan_tail_inputs(lens, s_max, nq, Hq, Hkv, d, seed):
+def _nan_tail_inputs(lens, s_max, nq, Hq, Hkv, d, seed, dtype=torch.bfloat16):
     gen = torch.Generator().manual_seed(seed)
     B = len(lens)
-    q = torch.randn(B, nq, Hq, d, generator=gen).to(torch.bfloat16)
-    k = torch.randn(B, s_max, Hkv, d, generator=gen).to(torch.bfloat16)
-    v = torch.randn(B, s_max, Hkv, d, generator=gen).to(torch.bfloat16)
+    q = torch.randn(B, nq, Hq, d, generator=gen).to(dtype)
+    k = torch.randn(B, s_max, Hkv, d, generator=gen).to(dtype)
+    v = torch.randn(B, s_max, Hkv, d, generator=gen).to(dtype)
     for b, L in enumerate(lens):   # cache positions past the sequence hold NaN
         k[b, max(L, 0):] = float("nan")
         v[b, max(L, 0):] = float("nan")
@@ -306,3 +306,65 @@ def test_one_long_pair_more_than_64_pieces():
     ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
     out, lse = run_gpu(inp, 0, torch.float32)
     assert_close(out, lse, *ref, "one pair, 256 blocks")
+
+
+# ------------------------------------------------------------------ fp16 inputs
+@functools.lru_cache(maxsize=2)
+def fp16_case(name):
+    cfg = workloads.CONFIGS[name]
+    inp = workloads.make_inputs(cfg, dtype=torch.float16)
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, causal=cfg.causal)
+    return cfg, inp.to(DEV), ref
+
+
+FP16 = [("llama8b", 0, torch.float16), ("llama8b", 1, torch.float16), ("spec", 0, torch.float16),
+        ("spec", 5, torch.float32), ("tiny", 4, torch.float16), ("ragged", 0, torch.float32)]
+
+
+@pytest.mark.parametrize("name,splits,out_dtype", FP16, ids=[f"{n}-s{s}-{str(o)[6:]}" for n, s, o in FP16])
+def test_fp16_inputs_full_size(name, splits, out_dtype):
+    """fp16 q, k, v (P enters the value MMA in fp16) at full config size,
+    with fp16 and fp32 outputs."""
+    cfg, inp, (ref_out, ref_lse) = fp16_case(name)
+    out, lse = run_gpu(inp, splits, out_dtype, cfg.causal)
+    assert out.dtype == out_dtype
+    assert_close(out, lse, ref_out, ref_lse, f"fp16 {name} splits={splits} out={out_dtype}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp16_edge_lengths_and_poisoned_tail(d):
+    lens = [1, 127, 128, 129, 4097, 0, 4]
+    q, k, v, sl = _nan_tail_inputs(lens, 4200, 4, 16, 2, d, seed=300 + d, dtype=torch.float16)
+    ref = oracle.decode(q, k, v, sl, causal=True)
+    for splits in (0, 3):
+        out, lse = run_gpu(workloads.DecodeInputs(None, q, k, v, sl, 1 / math.sqrt(d)).to(DEV), splits,
+                           torch.float16, True)
+        assert_close(out, lse, *ref, f"fp16 edge d={d} splits={splits}")
+
+
+def test_fp16_splitkv_then_combine_to_fp16():
+    cfg = workloads.shrink(workloads.CONFIGS["llama8b"], batch=3, seqlen=900)
+    inp = workloads.make_inputs(cfg, dtype=torch.float16)
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    d = inp.to(DEV)
+    B, nq, Hq, D = d.q.shape
+    S = 4
+    o_part = torch.empty((S, B, nq, Hq, D), device=DEV)
+    lse_part = torch.empty(S, B, nq, Hq, device=DEV)
+    g.gqa_decode_splitkv(d.q, d.k_cache, d.v_cache, d.seqlens, S, o_part, lse_part)
+    out = torch.empty(B, nq, Hq, D, dtype=torch.float16, device=DEV)
+    lse = torch.empty(B, nq, Hq, device=DEV)
+    g.gqa_decode_combine(o_part, lse_part, out, lse)
+    torch.cuda.synchronize()
+    assert_close(out, lse, *ref, "fp16 splitkv + combine")
+
+
+def test_mixed_types_are_rejected():
+    cfg = workloads.shrink(workloads.CONFIGS["llama8b"], batch=1, seqlen=256)
+    inp = workloads.make_inputs(cfg).to(DEV)
+    with pytest.raises(ValueError):
+        g.decode(inp.q.to(torch.float16), inp.k_cache, inp.v_cache, inp.seqlens)
+    # a 16-bit output of the other 16-bit type
+    with pytest.raises(g.GQAError) as e:
+        g.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, out_dtype=torch.float16)
+    assert e.value.status == g.GQA_ERR_UNSUPPORTED
