@@ -95,8 +95,7 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 // output element types (the values of gqa_dtype_t)
 constexpr int kOutBF16 = 0, kOutF32 = 1, kOutF16 = 2;
 
-constexpr int kThreads = 224;       // producer, QK issuer, PV issuer, 4 softmax warps
-constexpr int kSoftmaxThread0 = 96;  // first thread of the softmax warpgroup
+constexpr int kSoftmaxThread0 = 96;  // first thread of the (first) softmax warpgroup
 constexpr int kMaxSmemB = 512;       // sequences whose lengths are staged in shared memory
 constexpr int kMaxListItems = 128;   // work items of one CTA kept as a list in shared memory
 constexpr float kRescaleThreshold = 8.0f;
@@ -129,15 +128,27 @@ struct DecodeCfg {
   static constexpr int kQBytes = kChunks * NPAD * 128;       // one Q buffer
   static constexpr int kPBytes = 2 * NPAD * 128;             // one P buffer (two 64-position atoms)
   static constexpr int kOWidth = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // TMEM columns of O
+  // Softmax warpgroups.  With 32 columns the softmax is the slower side of
+  // the pipeline, and two warpgroups each take 16 of the columns (their own
+  // running max and sums, their own O columns and rows of P), so that twice
+  // as many warps hide its latencies.  Warps: producer, score-MMA issuer,
+  // value-MMA issuer, then 4 * kWGs softmax warps.
+  static constexpr int kWGs = NPAD == 32 ? 2 : 1;
+  static constexpr int kNC = NPAD / kWGs;  // columns per softmax warpgroup
+  static constexpr int kThreads = 96 + 128 * kWGs;
   // fixed part of shared memory after the ring
-  static constexpr int kXchgBytes = 2 * (4 * 4 + 4 * NPAD * 4);
+  static constexpr int kXchgBytes = kWGs * 2 * (4 * 4 + 4 * kNC * 4);
+  // head_dim 64 with two warpgroups: scratch for the epilogue's exchange of
+  // the stacked half-blocks (one warpgroup uses the P buffers, which the
+  // other may already be refilling)
+  static constexpr int kXoBytes = (kWGs == 2 && HEAD_DIM == 64) ? NPAD * 64 * 4 : 0;
   static constexpr int kListBytes = 16 + kMaxListItems * static_cast<int>(sizeof(WorkItem));
   static constexpr int kMiscBytes =
       (512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64 + kListBytes + 127) / 128 * 128;
   // output staging, two buffers: one item's rows (fp32 worst case), its LSEs,
   // its piece count
   static constexpr int kOutBytes = (NPAD * HEAD_DIM * 4 + 128 + 16 + 127) / 128 * 128;
-  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes + 2 * kOutBytes;
+  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes + 2 * kOutBytes + kXoBytes;
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // minus alignment slack
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kSlotBytes;
   // Four stages (two K, two V blocks) per SM keep enough bytes in flight
@@ -233,12 +244,15 @@ struct ItemSource {
 
 // IN_F16: q, k, v (and P) are fp16; otherwise bf16.
 template <int HEAD_DIM, int NPAD, bool IN_F16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DecodeCfg<HEAD_DIM, NPAD>::kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HEAD_DIM, NPAD>;
   constexpr int NS = Cfg::kStages;
   constexpr uint32_t NSK = Cfg::kStagesK, NSV = Cfg::kStagesV;  // K ring, then V ring
   constexpr int KCH = Cfg::kChunks;
+  constexpr int kThreads = Cfg::kThreads;
+  constexpr int NWG = Cfg::kWGs;  // softmax warpgroups
+  constexpr int NC = Cfg::kNC;    // columns per softmax warpgroup
   GQA_TRACE_SETUP();
 
   extern __shared__ uint8_t smem_raw[];
@@ -248,8 +262,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   uint8_t* pbuf = qbuf + 2 * Cfg::kQBytes;               // 2 x kPBytes
   uint8_t* misc = pbuf + 2 * Cfg::kPBytes;
   uint64_t* bar = reinterpret_cast<uint64_t*>(misc);     // 64 barrier words max
-  uint32_t* xflags = reinterpret_cast<uint32_t*>(misc + 512);         // [2][4]
-  float* xvals = reinterpret_cast<float*>(misc + 512 + 32);            // [2][4][NPAD]
+  // per softmax warpgroup: flags [2][4], then values [2][4][NC]
+  auto xflags_of = [&](int w) { return reinterpret_cast<uint32_t*>(misc + 512 + w * (Cfg::kXchgBytes / NWG)); };
+  auto xvals_of = [&](int w) { return reinterpret_cast<float*>(misc + 512 + w * (Cfg::kXchgBytes / NWG) + 32); };
   int32_t* s_len = reinterpret_cast<int32_t*>(misc + 512 + Cfg::kXchgBytes);  // [kMaxSmemB]
   int32_t* s_pre = s_len + kMaxSmemB;                                   // [kMaxSmemB + 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_pre + kMaxSmemB + 1);
@@ -261,6 +276,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   auto obuf_of = [&](int ob) -> uint8_t* { return misc + Cfg::kMiscBytes + ob * Cfg::kOutBytes; };
   auto lse_of = [&](int ob) -> float* { return reinterpret_cast<float*>(obuf_of(ob) + NPAD * HEAD_DIM * 4); };
   auto np_of = [&](int ob) -> int32_t* { return reinterpret_cast<int32_t*>(lse_of(ob) + 32); };
+  float* xo_buf = reinterpret_cast<float*>(obuf_of(0) + 2 * Cfg::kOutBytes);  // kXoBytes
 
   // barrier indices
   const uint32_t bar_base = ptx::smem_u32(bar);
@@ -289,15 +305,15 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ptx::mbar_init(BAR(Q_FULL + i), 1);
       ptx::mbar_init(BAR(Q_EMPTY + i), 1);
       ptx::mbar_init(BAR(S_FULL + i), 1);
-      ptx::mbar_init(BAR(S_EMPTY + i), 4);
-      ptx::mbar_init(BAR(P_FULL + i), 4);
+      ptx::mbar_init(BAR(S_EMPTY + i), 4 * NWG);  // one arrival per softmax warp
+      ptx::mbar_init(BAR(P_FULL + i), 4 * NWG);
       ptx::mbar_init(BAR(P_EMPTY + i), 1);
     }
     ptx::mbar_init(BAR(DRAIN), 1);
     ptx::mbar_init(BAR(DRAIN + 1), 1);
     ptx::mbar_init(BAR(PLAN_READY), 1);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(BAR(OUT_FULL + i), 1);
+      ptx::mbar_init(BAR(OUT_FULL + i), NWG);  // each warpgroup's staging done
       ptx::mbar_init(BAR(OUT_EMPTY + i), 1);
     }
     *abort_flag = 0;
@@ -673,6 +689,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int r = tq * 32 + lane;     // TMEM lane = KV row of S^T = row of O^T
     const uint32_t lane_addr = static_cast<uint32_t>(tq * 32) << 16;
     const int nv = p.nq * p.G;        // valid columns
+    const int wg = NWG == 1 ? 0 : (warp - 3) >> 2;  // this softmax warpgroup
+    const int c0 = wg * NC;                         // its first column
+    const int sm0 = kSoftmaxThread0 + 128 * wg;     // its first thread
+    const uint32_t xbar = 1u + 2u * static_cast<uint32_t>(wg);  // its named barrier
+    uint32_t* xflags = xflags_of(wg);
+    float* xvals = xvals_of(wg);
     bool local_abort = false;
     uint32_t xc = 0;                  // exchange counter
 
@@ -684,20 +706,20 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ++xc;
       if (lane == 0) xflags[buf * 4 + tq] = flags;
       if (with_vals) {
-        const int col = detail::transpose_col<NPAD>(lane);
-        if (NPAD == 32 || (lane & 1) == 0) xvals[(buf * 4 + tq) * NPAD + col] = val;
+        const int col = detail::transpose_col<NC>(lane);
+        if (NC == 32 || (lane & 1) == 0) xvals[(buf * 4 + tq) * NC + col] = val;
       }
-      ptx::named_barrier_sync(1, 128);
+      ptx::named_barrier_sync(xbar, 128);
       return xflags[buf * 4 + 0] | xflags[buf * 4 + 1] | xflags[buf * 4 + 2] | xflags[buf * 4 + 3];
     };
     // Per-column combination of the four warps' values of the last exchange,
     // read as 16-byte vectors.
-    auto xcombine = [&](float (&outv)[NPAD], bool is_max) {
-      const float4* base = reinterpret_cast<const float4*>(xvals + ((xc - 1) & 1u) * 4 * NPAD);
+    auto xcombine = [&](float (&outv)[NC], bool is_max) {
+      const float4* base = reinterpret_cast<const float4*>(xvals + ((xc - 1) & 1u) * 4 * NC);
 #pragma unroll
-      for (int c4 = 0; c4 < NPAD / 4; ++c4) {
-        const float4 a = base[0 * (NPAD / 4) + c4], b4 = base[1 * (NPAD / 4) + c4];
-        const float4 c = base[2 * (NPAD / 4) + c4], d4 = base[3 * (NPAD / 4) + c4];
+      for (int c4 = 0; c4 < NC / 4; ++c4) {
+        const float4 a = base[0 * (NC / 4) + c4], b4 = base[1 * (NC / 4) + c4];
+        const float4 c = base[2 * (NC / 4) + c4], d4 = base[3 * (NC / 4) + c4];
         if (is_max) {
           outv[4 * c4 + 0] = fmaxf(fmaxf(a.x, b4.x), fmaxf(c.x, d4.x));
           outv[4 * c4 + 1] = fmaxf(fmaxf(a.y, b4.y), fmaxf(c.y, d4.y));
@@ -717,7 +739,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     // joins the next exchange's flags.
     uint32_t k_out = 0;  // items staged
     auto wait_staging = [&]() -> bool {
-      if (threadIdx.x != kSoftmaxThread0) return true;
+      if (threadIdx.x != sm0) return true;
       if constexpr (!kPvStores) {
         ptx::bulk_wait_read_all();
         return true;
@@ -731,8 +753,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     // (or hands them to the value-MMA thread).
     auto hand_over = [&](const WorkItem& wi) {
       ptx::fence_proxy_async_smem();
-      ptx::named_barrier_sync(1, 128);
-      if (threadIdx.x == kSoftmaxThread0) {
+      ptx::named_barrier_sync(xbar, 128);
+      if (threadIdx.x == sm0) {
         if constexpr (kPvStores) ptx::mbar_arrive(BAR(OUT_FULL + (k_out & 1u)));
         else store_item(wi, static_cast<int>(k_out & 1u));
       }
@@ -751,27 +773,27 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (exchange(st_ok ? 0u : 2u, false, 0.f) & 2u) { aborted = true; break; }
         uint8_t* ob = obuf_of(static_cast<int>(k_out & 1u));
         if (r < HEAD_DIM) {
-          for (int n = 0; n < nv; ++n) {
+          for (int n = c0; n < c0 + NC && n < nv; ++n) {
             if (it.slot < 0 && p.out_dtype != kOutF32)
               reinterpret_cast<__nv_bfloat16*>(ob)[n * HEAD_DIM + r] = __float2bfloat16_rn(0.f);  // +0: all-zero bits
             else
               reinterpret_cast<float*>(ob)[n * HEAD_DIM + r] = 0.f;
           }
         }
-        if (r < nv) lse_of(static_cast<int>(k_out & 1u))[r] = -INFINITY;
+        if (r >= c0 && r < c0 + NC && r < nv) lse_of(static_cast<int>(k_out & 1u))[r] = -INFINITY;
         hand_over(it);
         continue;
       }
       const int L = it.L;
-      float m[NPAD], l[NPAD];
+      float m[NC], l[NC];  // this warpgroup's columns c0 + n
 #pragma unroll
-      for (int n = 0; n < NPAD; ++n) { m[n] = -INFINITY; l[n] = 0.f; }
+      for (int n = 0; n < NC; ++n) { m[n] = -INFINITY; l[n] = 0.f; }
 
       for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
         const bool first = (blk == it.blk_begin);
         const uint32_t sl = g & 1u;
         // ---- scores
-        float x[NPAD];
+        float x[NC];
         if (!local_abort)
           local_abort = !ptx::mbar_wait_bounded(BAR(S_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns);
         local_abort = __any_sync(0xffffffffu, local_abort);
@@ -780,16 +802,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (!local_abort) {
           const uint32_t s_col = sl ? kSCol1 : kSCol0;
 #pragma unroll
-          for (int c = 0; c < NPAD; c += 16) {
+          for (int c = 0; c < NC; c += 16) {
             float v16[16];
-            ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + s_col + c, v16);
+            ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + s_col + c0 + c, v16);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[c + i] = v16[i];
           }
         } else {
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) x[n] = -INFINITY;
+          for (int n = 0; n < NC; ++n) x[n] = -INFINITY;
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -807,8 +829,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         const bool row_valid = pos < L;
         bool need = false;
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) {
-          const bool vis = row_valid && n >= n_min && n < nv;
+        for (int n = 0; n < NC; ++n) {
+          const bool vis = row_valid && c0 + n >= n_min && c0 + n < nv;
           x[n] = vis ? x[n] * p.scale_log2 : -INFINITY;
           need |= x[n] > m[n] + kRescaleThreshold;
         }
@@ -818,7 +840,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 
         // ---- correction (only when some column's max moved past the threshold)
         if (fl & 1u) {
-          const float wmax = detail::transpose_reduce<NPAD, true>(x, lane);
+          const float wmax = detail::transpose_reduce<NC, true>(x, lane);
           if (!first && !local_abort) {
             // O may be rescaled only after PV(g-1) has landed
             local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u,
@@ -827,10 +849,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           local_abort = __any_sync(0xffffffffu, local_abort);
           const uint32_t f2 = exchange(local_abort ? 2u : 0u, true, wmax);
           if (f2 & 2u) { aborted = true; break; }
-          float alpha[NPAD], bmax[NPAD];
+          float alpha[NC], bmax[NC];
           xcombine(bmax, true);
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) {
+          for (int n = 0; n < NC; ++n) {
             const float mn = fmaxf(m[n], bmax[n]);
             const float ms = mn == -INFINITY ? 0.f : mn;
             alpha[n] = ptx::ex2_approx(m[n] - ms);
@@ -838,24 +860,30 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
             l[n] *= alpha[n];
           }
           if (!first) {
+            // this warpgroup's O columns: c0 + [0, NC), and for head_dim 64
+            // the same columns of the second stacked half at +NPAD
             ptx::tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < Cfg::kOWidth; c += 16) {
-              float o16[16];
-              ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + kOCol + c, o16);
-              ptx::tmem_wait_ld();
+            for (int h2 = 0; h2 < Cfg::kOWidth / NPAD; ++h2) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o16[i] *= alpha[(c + i) % NPAD];
-              ptx::tmem_st_32x32b_x16(tmem_base + lane_addr + kOCol + c, o16);
+              for (int c = 0; c < NC; c += 16) {
+                const uint32_t col = kOCol + static_cast<uint32_t>(h2 * NPAD + c0 + c);
+                float o16[16];
+                ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + col, o16);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o16[i] *= alpha[c + i];
+                ptx::tmem_st_32x32b_x16(tmem_base + lane_addr + col, o16);
+              }
             }
             ptx::tmem_wait_st();
           }
         }
 
         // ---- probabilities; the denominator is accumulated per lane
-        float pr[NPAD];
+        float pr[NC];
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) {
+        for (int n = 0; n < NC; ++n) {
           const float ms = m[n] == -INFINITY ? 0.f : m[n];
           pr[n] = ptx::ex2_approx(x[n] - ms);
           l[n] += pr[n];
@@ -870,18 +898,19 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           uint8_t* pb = pbuf + sl * Cfg::kPBytes + (r >> 6) * (NPAD * 128);
           const int chunk = (r & 63) >> 3, within = (r & 7) * 2;
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) {
-            const int sw = chunk ^ (n & 7);
+          for (int n = 0; n < NC; ++n) {
+            const int ng = c0 + n;
+            const int sw = chunk ^ (ng & 7);
             if constexpr (IN_F16)
-              *reinterpret_cast<__half*>(pb + n * 128 + sw * 16 + within) = __float2half_rn(pr[n]);
+              *reinterpret_cast<__half*>(pb + ng * 128 + sw * 16 + within) = __float2half_rn(pr[n]);
             else
-              *reinterpret_cast<__nv_bfloat16*>(pb + n * 128 + sw * 16 + within) = __float2bfloat16_rn(pr[n]);
+              *reinterpret_cast<__nv_bfloat16*>(pb + ng * 128 + sw * 16 + within) = __float2bfloat16_rn(pr[n]);
           }
           // Tail block: V rows past the sequence end hold whatever the cache
           // holds there; zero them so that 0 * garbage cannot poison O.
           const int tail_rows = L - blk * kBlockN;
           const int cap_rows = plan.max_seqlen - blk * kBlockN;
-          if (tail_rows < kBlockN && cap_rows > tail_rows) {
+          if (wg == 0 && tail_rows < kBlockN && cap_rows > tail_rows) {
             // Wait for V(g) to land.  PV(g-2) is done, so V(g - NSV) was
             // consumed and this parity wait cannot pass a phase early.
             const uint32_t stage = NSK + g % NSV;
@@ -911,40 +940,45 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (!local_abort)
         local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag, p.timeout_ns);
       local_abort = __any_sync(0xffffffffu, local_abort);
-      const float lsum = detail::transpose_reduce<NPAD, false>(l, lane);
+      const float lsum = detail::transpose_reduce<NC, false>(l, lane);
       const bool st_ok = wait_staging();  // staging buffer free after f3
       const uint32_t f3 = exchange((local_abort || !st_ok) ? 2u : 0u, true, lsum);
       if (f3 & 2u) { aborted = true; break; }
-      float lt[NPAD];
+      float lt[NC];
       xcombine(lt, false);
 
       ptx::tc_fence_after();
-      float o[Cfg::kOWidth];
+      constexpr int kHalves = Cfg::kOWidth / NPAD;  // 2 for head_dim 64 (stacked half-blocks)
+      float o[kHalves * NC];
 #pragma unroll
-      for (int c = 0; c < Cfg::kOWidth; c += 16) {
-        float o16[16];
-        ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + kOCol + c, o16);
-        ptx::tmem_wait_ld();
+      for (int h2 = 0; h2 < kHalves; ++h2) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[c + i] = o16[i];
+        for (int c = 0; c < NC; c += 16) {
+          float o16[16];
+          ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + kOCol + static_cast<uint32_t>(h2 * NPAD + c0 + c), o16);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[h2 * NC + c + i] = o16[i];
+        }
       }
       ptx::tc_fence_before();
       int d_row = r;
       bool writer = true;
       if constexpr (HEAD_DIM == 64) {
         // lanes 64..127 hold the second half-block's contribution in columns [N, 2N)
-        float* xo = reinterpret_cast<float*>(pbuf);  // both P buffers are idle here
+        // (one warpgroup: both P buffers are idle here; two: own scratch)
+        float* xo = NWG == 1 ? reinterpret_cast<float*>(pbuf) : xo_buf;
         // [n][row] layout: the 32 lanes of a warp touch 32 consecutive words
         if (r >= 64) {
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) xo[n * 64 + (r - 64)] = o[NPAD + n];
+          for (int n = 0; n < NC; ++n) xo[(c0 + n) * 64 + (r - 64)] = o[NC + n];
         }
-        ptx::named_barrier_sync(1, 128);
+        ptx::named_barrier_sync(xbar, 128);
         if (r < 64) {
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) o[n] += xo[n * 64 + r];
+          for (int n = 0; n < NC; ++n) o[n] += xo[(c0 + n) * 64 + r];
         }
-        ptx::named_barrier_sync(1, 128);  // xo is read before P is rewritten
+        ptx::named_barrier_sync(xbar, 128);  // xo is read before P is rewritten
         writer = r < 64;
       }
       // Outputs go to shared memory in their global layout (row n = t*G + g
@@ -955,25 +989,26 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         const bool out16 = it.slot < 0 && p.out_dtype != kOutF32;
         uint8_t* obuf = obuf_of(static_cast<int>(k_out & 1u));
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) {
+        for (int n = 0; n < NC; ++n) {
           const float inv = lt[n] > 0.f ? ptx::rcp_approx(lt[n]) : 0.f;
           const float val = o[n] * inv;
-          if (n < nv) {
+          const int ng = c0 + n;
+          if (ng < nv) {
             if (out16) {
               if constexpr (IN_F16)
-                reinterpret_cast<__half*>(obuf)[n * HEAD_DIM + d_row] = __float2half_rn(val);
+                reinterpret_cast<__half*>(obuf)[ng * HEAD_DIM + d_row] = __float2half_rn(val);
               else
-                reinterpret_cast<__nv_bfloat16*>(obuf)[n * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
+                reinterpret_cast<__nv_bfloat16*>(obuf)[ng * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
             } else {
-              reinterpret_cast<float*>(obuf)[n * HEAD_DIM + d_row] = val;
+              reinterpret_cast<float*>(obuf)[ng * HEAD_DIM + d_row] = val;
             }
           }
         }
-        if (d_row < nv) {
+        if (d_row >= c0 && d_row < c0 + NC && d_row < nv) {
           float lt_n = 0.f, m_n = 0.f;
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n)
-            if (n == d_row) { lt_n = lt[n]; m_n = m[n]; }
+          for (int n = 0; n < NC; ++n)
+            if (c0 + n == d_row) { lt_n = lt[n]; m_n = m[n]; }
           lse_of(static_cast<int>(k_out & 1u))[d_row] =
               lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
         }

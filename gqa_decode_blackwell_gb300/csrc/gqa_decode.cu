@@ -232,7 +232,7 @@ gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodePar
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(static_cast<unsigned>(p.plan.num_ctas), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
