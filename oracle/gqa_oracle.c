@@ -86,9 +86,11 @@ static double fp16_to_double(uint16_t h) {
 }
 
 /* One input element, widened to double. */
-double gqa_oracle_elem(int in_fp16, uint16_t bits) {
+static inline double elem_to_double(int in_fp16, uint16_t bits) {
   return in_fp16 ? fp16_to_double(bits) : bf16_to_double(bits);
 }
+
+double gqa_oracle_elem(int in_fp16, uint16_t bits) { return elem_to_double(in_fp16, bits); }
 
 typedef struct {
   const gqa_oracle_shape* sh;
@@ -158,12 +160,12 @@ static void* oracle_rows(void* arg) {
       continue;
     }
     const uint16_t* qp = job->q + (size_t)row * d; /* q is [B, nq, Hq, d] */
-    for (int x = 0; x < d; ++x) qrow[x] = gqa_oracle_elem(sh->in_fp16, qp[x]);
+    for (int x = 0; x < d; ++x) qrow[x] = elem_to_double(sh->in_fp16, qp[x]);
     /* pass 1: scores and their max */
     double M = -INFINITY;
     for (int j = lo; j < hi; ++j) {
       double dot = 0.0;
-      for (int x = 0; x < d; ++x) dot += qrow[x] * gqa_oracle_elem(sh->in_fp16, job->k[cache_index(sh, b, j, h, x)]);
+      for (int x = 0; x < d; ++x) dot += qrow[x] * elem_to_double(sh->in_fp16, job->k[cache_index(sh, b, j, h, x)]);
 #if ORACLE_MUTANT == 1 /* mistake: scale dropped */
       s[j] = dot;
 #else
@@ -186,7 +188,7 @@ static void* oracle_rows(void* arg) {
 #else
       const uint16_t* vsrc = job->v;
 #endif
-      for (int x = 0; x < d; ++x) acc[x] += w * gqa_oracle_elem(sh->in_fp16, vsrc[cache_index(sh, b, j, h, x)]);
+      for (int x = 0; x < d; ++x) acc[x] += w * elem_to_double(sh->in_fp16, vsrc[cache_index(sh, b, j, h, x)]);
     }
 #if ORACLE_MUTANT == 7 /* mistake: no normalisation */
     for (int x = 0; x < d; ++x) o[x] = acc[x];
