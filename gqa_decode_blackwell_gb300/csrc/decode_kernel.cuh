@@ -333,7 +333,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     ptx::griddep_wait();
     if (lane == 0) GQA_TRACE_EVENT(TR_START, 0);
     if (lens_in_smem) {
-      // clamped lengths and the exclusive prefix sums of their block counts
+      // clamped lengths and the exclusive prefix sums of their pairs' units
       for (int i = lane; i < B; i += 32) {
         const int raw = p.seqlens[i];
         const int L = clamp_len(raw, plan.max_seqlen);
@@ -344,7 +344,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       int run = 0;
       for (int base = 0; base < B; base += 32) {
         const int i = base + lane;
-        const int nb = i < B ? num_blocks(s_len[i]) : 0;
+        const int nb = i < B ? pair_units(num_blocks(s_len[i]), plan.item_units) : 0;
         int incl = nb;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {

@@ -130,6 +130,12 @@ int auto_splits(long long pairs, int nblk, int rows_per_pair, int head_dim, int 
   return best_s;
 }
 
+// Item units X of the balanced plan: a work item's fixed cost in blocks.
+// Per-CTA traces on GB300 put a CTA's time at about a + b * blocks + c * items
+// with c / b = 1.5 (16 query columns) to 2.5 (32); timing X = 0..3 on the
+// Llama-shaped, speculative and ragged workloads, X = 3 was best or tied on each.
+constexpr int kItemUnits = 3;
+
 HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_partial) {
   HostPlan hp;
   std::memset(&hp, 0, sizeof hp);
@@ -140,9 +146,12 @@ HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_parti
   const int nblk_cap = num_blocks(d->max_seqlen);
   const long long pairs = static_cast<long long>(d->batch) * d->kv_heads;
   const int rows_per_pair = d->q_tokens * (d->q_heads / d->kv_heads);
-  if (num_splits == 0 && d->batch <= kMaxSmemB) {
+  // the balanced plan keeps per-sequence unit prefix sums in int32
+  const bool pre_fits = static_cast<long long>(d->batch) * pair_units(nblk_cap, kItemUnits) <= 0x7fffffffLL;
+  if (num_splits == 0 && d->batch <= kMaxSmemB && pre_fits) {
     pp.mode = PLAN_BALANCED;
-    long long units_cap = pairs * nblk_cap;
+    pp.item_units = kItemUnits;
+    long long units_cap = pairs * pair_units(nblk_cap, pp.item_units);
     if (units_cap < 1) units_cap = 1;
     pp.num_ctas = static_cast<int>(units_cap < sm ? units_cap : sm);
     pp.num_splits = 0;
@@ -551,7 +560,8 @@ gqa_status_t gqa_decode_plan(const gqa_desc_t* desc, const int32_t* seqlens_host
   std::vector<int32_t> clamped(static_cast<size_t>(B > 0 ? B : 1)), pre(static_cast<size_t>(B) + 1, 0);
   for (int b = 0; b < B; ++b) {
     clamped[b] = clamp_len(seqlens_host[b], desc->max_seqlen);
-    pre[b + 1] = pre[b] + num_blocks(clamped[b]);
+    pre[b + 1] = pre[b] + (hp.pp.mode == PLAN_BALANCED ? pair_units(num_blocks(clamped[b]), hp.pp.item_units)
+                                                        : num_blocks(clamped[b]));
   }
   int64_t n = 0;
   if (desc->batch > 0) {

@@ -19,11 +19,16 @@
 //  * PLAN_BALANCED: the U units of all pairs, ordered (b, h, block), are cut
 //    into C' = min(C, U) equal contiguous ranges, one per CTA (CTA c < C'
 //    owns units [floor(cU/C'), floor((c+1)U/C')), at least one each; CTAs
-//    c >= C' own nothing).  Because no range is empty, the CTAs touching a
-//    pair are consecutive.  A pair that falls inside one CTA is
-//    written as final output; a pair cut by CTA boundaries gets one partial
-//    per CTA touching it, in slot (c - first CTA of the pair), and the CTA
-//    that holds its first unit publishes the piece count for the combine.
+//    c >= C' own nothing).  Each non-empty pair also counts X = item_units
+//    units before its blocks, which hold no work: a work item costs a fixed
+//    time (Q load, pipeline fill, epilogue) worth a few blocks, so a CTA
+//    whose range takes in the start of a pair -- and with it one more item --
+//    gets X fewer blocks.  Because no range is empty, the CTAs touching a
+//    pair's blocks are consecutive.  A pair whose blocks fall inside one CTA
+//    is written as final output; a pair cut by CTA boundaries gets one
+//    partial per CTA touching its blocks, in slot (c - first such CTA), and
+//    the CTA holding its first block publishes the piece count for the
+//    combine.
 //    Pairs of empty sequences belong to the CTA whose range contains their
 //    (zero-length) start; trailing ones to CTA C' - 1.
 #pragma once
@@ -50,6 +55,7 @@ struct PlanParams {
   int min_blocks;     // PLAN_SPLITS: minimum blocks per split
   int force_partial;  // PLAN_SPLITS: write partials even when S == 1
   int num_ctas;       // C: CTAs of the persistent grid
+  int item_units;     // PLAN_BALANCED: X, the units a pair's item costs before its blocks
 };
 
 struct WorkItem {
@@ -64,6 +70,8 @@ struct WorkItem {
 
 GQA_HD int clamp_len(int L, int s_max) { return L < 0 ? 0 : (L > s_max ? s_max : L); }
 GQA_HD int num_blocks(int L) { return (L + kBlockN - 1) / kBlockN; }
+// Units of one pair in the balanced plan: its blocks plus X item units (none when empty).
+GQA_HD int pair_units(int nblk, int X) { return nblk > 0 ? nblk + X : 0; }
 
 // floor(a * b / c) for a, b >= 0 and c > 0.  GPUs emulate 64-bit division in
 // software, so the common case where everything fits in 32 bits takes the
@@ -121,18 +129,19 @@ struct SplitIter {
   }
 };
 
-// Contiguous equal ranges of units.  `lens` are clamped lengths and `pre` the
-// exclusive prefix sums of their block counts (B + 1 entries).
+// Contiguous equal ranges of units.  `lens` are clamped lengths and `pre`
+// (B + 1 entries) the exclusive prefix sums of the units of one pair of each
+// sequence: its blocks + X when it is non-empty, 0 when it is empty.
 struct BalancedIter {
   const int32_t* lens;
   const int32_t* pre;
   long long U, lo, hi;
-  int B, H;
+  int B, H, X;
   int b, h, cta, C;  // C: effective CTA count min(num_ctas, U), at least 1
 
   GQA_HD void init(const PlanParams& p, const int32_t* l, const int32_t* prefix, int c) {
     lens = l; pre = prefix; cta = c;
-    B = p.batch; H = p.kv_heads;
+    B = p.batch; H = p.kv_heads; X = p.item_units;
     U = static_cast<long long>(H) * pre[B];
     C = U <= 0 ? 1 : (U < p.num_ctas ? static_cast<int>(U) : p.num_ctas);
     if (c >= C) {  // this CTA owns nothing
@@ -158,7 +167,7 @@ struct BalancedIter {
   __device__ __forceinline__ void init_warp(const PlanParams& p, const int32_t* l, const int32_t* prefix, int c,
                                             int lane) {
     lens = l; pre = prefix; cta = c;
-    B = p.batch; H = p.kv_heads;
+    B = p.batch; H = p.kv_heads; X = p.item_units;
     U = static_cast<long long>(H) * pre[B];
     C = U <= 0 ? 1 : (U < p.num_ctas ? static_cast<int>(U) : p.num_ctas);
     if (c >= C) {
@@ -197,13 +206,12 @@ struct BalancedIter {
   }
   GQA_HD bool next(WorkItem& it) {
     while (b < B) {
-      const int nblk = pre[b + 1] - pre[b];
-      const long long u_first = static_cast<long long>(H) * pre[b] + static_cast<long long>(h) * nblk;
-      const long long u_end = u_first + nblk;
-      if (nblk == 0) {
-        const bool owned = (u_first >= lo && u_first < hi) || (u_first == U && cta == C - 1);
+      const int vl = pre[b + 1] - pre[b];  // units of each pair of sequence b
+      const long long v_first = static_cast<long long>(H) * pre[b] + static_cast<long long>(h) * vl;
+      if (vl == 0) {
+        const bool owned = (v_first >= lo && v_first < hi) || (v_first == U && cta == C - 1);
         if (!owned) {
-          if (u_first >= hi) return false;
+          if (v_first >= hi) return false;
           advance();
           continue;
         }
@@ -213,7 +221,10 @@ struct BalancedIter {
         advance();
         return true;
       }
-      if (u_first >= hi) return false;
+      if (v_first >= hi) return false;
+      // the pair's blocks: units [u_first, u_end), after its X item units
+      const long long u_first = v_first + X;
+      const long long u_end = v_first + vl;
       const long long pl = u_first > lo ? u_first : lo;
       const long long ph = u_end < hi ? u_end : hi;
       if (pl >= ph) { advance(); continue; }

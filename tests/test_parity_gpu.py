@@ -297,8 +297,8 @@ def test_batch_larger_than_shared_length_table(splits):
 
 def test_one_long_pair_more_than_64_pieces():
     """One sequence on one KV head, 256 blocks over 152 CTAs: the balanced plan
-    cuts it into 152 pieces, more than the 64 the combine keeps in registers,
-    so the combine takes its many-splits loop."""
+    cuts it into more pieces than the 64 the combine keeps in registers, so
+    the combine takes its many-splits loop."""
     inp = _random_batch(1, 32768, 1, 4, 1, 128, seed=41, lo=32768)
     desc = g.make_desc(inp.q, inp.k_cache)
     C, mode, slots, items = g.gqa_decode_plan(desc, inp.seqlens.tolist(), 0, 0)

@@ -25,14 +25,31 @@ def _blocks(L):
     return (max(L, 0) + 127) // 128
 
 
-def check_balanced(seqlens, Hkv, s_max, sm):
+def _units(nblk, X):
+    return nblk + X if nblk > 0 else 0
+
+
+def check_balanced(seqlens, Hkv, s_max, sm, X=3):
+    """Balanced plan: every pair costs its blocks plus X item units; the
+    units, in pair order (batch-major), are cut into C contiguous ranges."""
     desc = _desc(len(seqlens), Hkv, s_max)
     C, mode, slots, items = g.gqa_decode_plan(desc, seqlens, 0, sm)
     assert mode == 1
     lens = [min(max(int(L), 0), s_max) for L in seqlens]
-    U = sum(_blocks(L) for L in lens) * Hkv
-    assert C == max(1, min(sm, len(lens) * Hkv * _blocks(s_max)))
+    U = sum(_units(_blocks(L), X) for L in lens) * Hkv
+    assert C == max(1, min(sm, len(lens) * Hkv * _units(_blocks(s_max), X)))
     C_eff = max(1, min(C, U))
+
+    def cta_of(u):  # the largest c with floor(c * U / C_eff) <= u
+        return ((u + 1) * C_eff - 1) // U
+    # unit order: pair (b, h) starts at v_first, its X item units come first
+    v_first, v = {}, 0
+    for b, L in enumerate(lens):
+        for h in range(Hkv):
+            v_first[(b, h)] = v
+            v += _units(_blocks(L), X)
+    assert v == U
+    vload = collections.Counter(cta_of(u) for u in range(U))
     cover = collections.Counter()
     per_pair = collections.defaultdict(list)
     per_cta = collections.Counter()
@@ -41,6 +58,7 @@ def check_balanced(seqlens, Hkv, s_max, sm):
         per_cta[c] += b1 - b0
         for blk in range(b0, b1):
             cover[(b, h, blk)] += 1
+            assert cta_of(v_first[(b, h)] + X + blk) == c
     # every unit exactly once
     expect = {(b, h, k) for b, L in enumerate(lens) for h in range(Hkv) for k in range(_blocks(L))}
     assert set(cover) == expect and all(v == 1 for v in cover.values())
@@ -62,12 +80,12 @@ def check_balanced(seqlens, Hkv, s_max, sm):
             assert ordered[0][1] == 0 and ordered[-1][2] == _blocks(L)
             for a, z in zip(ordered, ordered[1:]):
                 assert a[2] == z[1]
-    # only the first C_eff CTAs work; their loads differ by at most one block
+    # only the first C_eff CTAs work; their loads in units differ by at most one
     assert all(c < C_eff for c in per_cta)
-    loads = [per_cta.get(c, 0) for c in range(C_eff)]
     if U > 0:
+        loads = [vload.get(c, 0) for c in range(C_eff)]
         assert max(loads) - min(loads) <= 1
-        assert sum(loads) == U
+        assert sum(per_cta.values()) == U - X * Hkv * sum(1 for L in lens if L > 0)
 
 
 @pytest.mark.parametrize("seed", range(24))
@@ -131,9 +149,19 @@ def test_auto_falls_back_to_splits_for_huge_batches():
 
 
 def test_balanced_plan_can_exceed_64_pieces_per_pair():
-    """A long sequence on few KV heads is cut over every CTA: 152 pieces for
-    one pair, which the combine must merge beyond its 64-slot fast path."""
+    """A long sequence on few KV heads is cut over (nearly) every CTA: far
+    more than 64 pieces for one pair, which the combine must merge beyond its
+    64-slot fast path."""
     C, mode, slots, items = g.gqa_decode_plan(_desc(1, 1, 32768), [32768], 0, 152)
     assert mode == 1 and slots == 152
-    assert max(int(r[7]) for r in items) == 152
+    assert 140 <= max(int(r[7]) for r in items) <= 152
     check_balanced([32768], 1, 32768, 152)
+
+
+def test_balanced_plan_needs_int32_prefix_sums():
+    """512 sequences of up to 2^30 positions would overflow the balanced
+    plan's int32 prefix sums of units: the fixed-splits plan takes over."""
+    C, mode, slots, items = g.gqa_decode_plan(_desc(512, 1, 1 << 30), [1] * 512, 0, 152, max_items=0)
+    assert mode == 0
+    C, mode, slots, items = g.gqa_decode_plan(_desc(512, 1, 1 << 20), [1] * 512, 0, 152, max_items=0)
+    assert mode == 1
