@@ -291,11 +291,13 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   const bool lens_in_smem = B <= kMaxSmemB;
 
   // ---------------------------------------------------------------- set-up
-  // The producer warp only needs the barriers and the work plan: it computes
-  // the plan itself right after the grid dependency, publishes it through
-  // PLAN_READY and starts streaming, while the other warps allocate TMEM and
-  // zero the padding of the MMA operand buffers.
-  const int PLAN_READY = DRAIN + 2, OUT_FULL = DRAIN + 3, OUT_EMPTY = DRAIN + 5;
+  // Right after the grid dependency the producer warp stages the clamped
+  // lengths and their unit prefix sums (PRE_READY), finds its first item and
+  // starts streaming, walking the plan's iterator itself.  Meanwhile warp 2
+  // expands the same plan into the shared item list the other roles read
+  // (PLAN_READY), and the rest allocate TMEM and zero the padding of the MMA
+  // operand buffers.
+  const int PLAN_READY = DRAIN + 2, OUT_FULL = DRAIN + 3, OUT_EMPTY = DRAIN + 5, PRE_READY = DRAIN + 7;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       ptx::mbar_init(BAR(RING_FULL + i), 1);
@@ -312,6 +314,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     ptx::mbar_init(BAR(DRAIN), 1);
     ptx::mbar_init(BAR(DRAIN + 1), 1);
     ptx::mbar_init(BAR(PLAN_READY), 1);
+    ptx::mbar_init(BAR(PRE_READY), 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(BAR(OUT_FULL + i), NWG);  // each warpgroup's staging done
       ptx::mbar_init(BAR(OUT_EMPTY + i), 1);
@@ -324,7 +327,55 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   }
   __syncthreads();  // barriers initialised
 
+  // This CTA's work items, 32 candidates at a time (one per lane), written to
+  // the shared list by the 32 lanes of one warp.  Owned items form a
+  // contiguous run of candidates (pairs from the first one at or after this
+  // CTA's first unit; split items c, c + C, ...).
+  auto build_list = [&](int lane) {
+    WorkIter base_it;
+    base_it.init_warp(plan, lens_in_smem ? s_len : p.seqlens, s_len, s_pre, blockIdx.x, lane);
+    const bool balanced = plan.mode == PLAN_BALANCED;
+    long long p0 = 0, total = 0;
+    if (balanced) {
+      p0 = static_cast<long long>(base_it.bal.b) * plan.kv_heads + base_it.bal.h;
+      total = static_cast<long long>(B) * plan.kv_heads;
+    } else {
+      total = static_cast<long long>(B) * plan.kv_heads * plan.num_splits;
+    }
+    int count = 0;
+    for (int chunk = 0;; chunk += 32) {
+      WorkItem w;
+      bool owned = false;
+      if (balanced) {
+        const long long pr = p0 + chunk + lane;
+        if (pr < total && base_it.bal.b < B) {
+          BalancedIter bi = base_it.bal;
+          bi.b = static_cast<int>(pr / plan.kv_heads);
+          bi.h = static_cast<int>(pr - static_cast<long long>(bi.b) * plan.kv_heads);
+          // next() returns the first owned pair at or after this one: this
+          // candidate is owned iff it returns the candidate itself
+          owned = bi.next(w) && (static_cast<long long>(w.b) * plan.kv_heads + w.h == pr);
+        }
+      } else {
+        const long long wi = blockIdx.x + static_cast<long long>(chunk + lane) * plan.num_ctas;
+        if (wi < total) {
+          SplitIter si = base_it.s;
+          si.w = wi;
+          owned = si.next(w);
+        }
+      }
+      const unsigned mask = __ballot_sync(0xffffffffu, owned);
+      const int run = (~mask == 0u) ? 32 : __ffs(~mask) - 1;  // leading owned candidates
+      if (owned && lane < run && count + lane < kMaxListItems) list_items[count + lane] = w;
+      count += run;
+      if (run < 32) break;
+    }
+    if (lane == 0) list_hdr[0] = count <= kMaxListItems ? count : -1;
+    __threadfence_block();
+  };
+
   uint32_t tmem_base = 0;
+  WorkIter prod_it;  // the producer's own walk over the plan (warp 0)
   if (warp == 0) {
     // Warm L2 with the lengths while the previous kernel finishes: a prefetch
     // returns no data, so it cannot observe a value that kernel still writes.
@@ -355,57 +406,11 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         run += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0) s_pre[B] = run;
-      __threadfence_block();
     }
+    __threadfence_block();
     __syncwarp();
-    // This CTA's work items, 32 candidates at a time (one per lane).  Owned
-    // items form a contiguous run of candidates (pairs from the first one at
-    // or after this CTA's first unit; split items c, c + C, ...).
-    {
-      const int32_t* lens_r = lens_in_smem ? s_len : p.seqlens;
-      WorkIter base_it;
-      base_it.init_warp(plan, lens_r, s_len, s_pre, blockIdx.x, lane);
-      const bool balanced = plan.mode == PLAN_BALANCED;
-      long long p0 = 0, total = 0;
-      if (balanced) {
-        p0 = static_cast<long long>(base_it.bal.b) * plan.kv_heads + base_it.bal.h;
-        total = static_cast<long long>(B) * plan.kv_heads;
-      } else {
-        total = static_cast<long long>(B) * plan.kv_heads * plan.num_splits;
-      }
-      int count = 0;
-      for (int chunk = 0;; chunk += 32) {
-        WorkItem w;
-        bool owned = false;
-        if (balanced) {
-          const long long pr = p0 + chunk + lane;
-          if (pr < total && base_it.bal.b < B) {
-            BalancedIter bi = base_it.bal;
-            bi.b = static_cast<int>(pr / plan.kv_heads);
-            bi.h = static_cast<int>(pr - static_cast<long long>(bi.b) * plan.kv_heads);
-            // next() returns the first owned pair at or after this one: this
-            // candidate is owned iff it returns the candidate itself
-            owned = bi.next(w) && (static_cast<long long>(w.b) * plan.kv_heads + w.h == pr);
-          }
-        } else {
-          const long long wi = blockIdx.x + static_cast<long long>(chunk + lane) * plan.num_ctas;
-          if (wi < total) {
-            SplitIter si = base_it.s;
-            si.w = wi;
-            owned = si.next(w);
-          }
-        }
-        const unsigned mask = __ballot_sync(0xffffffffu, owned);
-        const int run = (~mask == 0u) ? 32 : __ffs(~mask) - 1;  // leading owned candidates
-        if (owned && lane < run && count + lane < kMaxListItems) list_items[count + lane] = w;
-        count += run;
-        if (run < 32) break;
-      }
-      if (lane == 0) list_hdr[0] = count <= kMaxListItems ? count : -1;
-      __threadfence_block();
-    }
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(BAR(PLAN_READY));
+    if (lane == 0) ptx::mbar_arrive(BAR(PRE_READY));  // lengths and prefix sums staged
+    prod_it.init_warp(plan, lens_in_smem ? s_len : p.seqlens, s_len, s_pre, blockIdx.x, lane);
   } else {
     if (warp == 1) {
       ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -427,6 +432,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     ptx::fence_proxy_async_smem();
     // Outputs and workspace may still be read by the previous kernel.
     ptx::griddep_wait();
+    if (warp == 2) {
+      if (ptx::mbar_wait_bounded(BAR(PRE_READY), 0, abort_flag, p.timeout_ns)) {
+        build_list(lane);
+      } else {
+        detail::set_error(kErrTimeout, abort_flag);
+        if (lane == 0) list_hdr[0] = 0;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(BAR(PLAN_READY));
+    }
     if (!ptx::mbar_wait_bounded(BAR(PLAN_READY), 0, abort_flag, p.timeout_ns))
       detail::set_error(kErrTimeout, abort_flag);
     ptx::tc_fence_before();
@@ -521,10 +536,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
         return true;
       };
-      ItemSource iter;
-      iter.init(list_hdr, list_items, plan, lens_raw, s_len, s_pre);
       WorkItem it;
-      while (ok && iter.next(it)) {
+      while (ok && prod_it.next(it)) {
         if (it.blk_begin >= it.blk_end) continue;
         GQA_TRACE_EVENT(TR_PROD_PLAN, static_cast<uint32_t>(kq));
         const int qb = kq & 1;
