@@ -129,19 +129,20 @@ struct DecodeCfg {
   static constexpr int kPBytes = 2 * NPAD * 128;             // one P buffer (two 64-position atoms)
   static constexpr int kOWidth = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // TMEM columns of O
   // Softmax warpgroups.  With 32 columns the softmax is the slower side of
-  // the pipeline, and two warpgroups each take 16 of the columns (their own
-  // running max and sums, their own O columns and rows of P), so that twice
-  // as many warps hide its latencies.  Warps: producer, score-MMA issuer,
-  // value-MMA issuer, then 4 * kWGs softmax warps.
-  static constexpr int kWGs = NPAD == 32 ? 2 : 1;
+  // the pipeline, and four warpgroups each take 8 of the columns (their own
+  // running max and sums, their own O columns and rows of P), so that four
+  // times as many warps hide its latencies (measured on GB300: faster than
+  // two warpgroups of 16 columns, which were faster than one).  Warps:
+  // producer, score-MMA issuer, value-MMA issuer, then 4 * kWGs softmax warps.
+  static constexpr int kWGs = NPAD == 32 ? 4 : 1;
   static constexpr int kNC = NPAD / kWGs;  // columns per softmax warpgroup
   static constexpr int kThreads = 96 + 128 * kWGs;
   // fixed part of shared memory after the ring
   static constexpr int kXchgBytes = kWGs * 2 * (4 * 4 + 4 * kNC * 4);
-  // head_dim 64 with two warpgroups: scratch for the epilogue's exchange of
+  // head_dim 64 with several warpgroups: scratch for the epilogue's exchange of
   // the stacked half-blocks (one warpgroup uses the P buffers, which the
   // other may already be refilling)
-  static constexpr int kXoBytes = (kWGs == 2 && HEAD_DIM == 64) ? NPAD * 64 * 4 : 0;
+  static constexpr int kXoBytes = (kWGs > 1 && HEAD_DIM == 64) ? NPAD * 64 * 4 : 0;
   static constexpr int kListBytes = 16 + kMaxListItems * static_cast<int>(sizeof(WorkItem));
   static constexpr int kMiscBytes =
       (512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64 + kListBytes + 127) / 128 * 128;
@@ -253,6 +254,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int kThreads = Cfg::kThreads;
   constexpr int NWG = Cfg::kWGs;  // softmax warpgroups
   constexpr int NC = Cfg::kNC;    // columns per softmax warpgroup
+  constexpr int CW = NC < 16 ? NC : 16;  // columns per TMEM load
   GQA_TRACE_SETUP();
 
   extern __shared__ uint8_t smem_raw[];
@@ -719,8 +721,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ++xc;
       if (lane == 0) xflags[buf * 4 + tq] = flags;
       if (with_vals) {
+        // after a transpose-reduce, 32 / NC consecutive lanes share a column
         const int col = detail::transpose_col<NC>(lane);
-        if (NC == 32 || (lane & 1) == 0) xvals[(buf * 4 + tq) * NC + col] = val;
+        if ((lane & (32 / NC - 1)) == 0) xvals[(buf * 4 + tq) * NC + col] = val;
       }
       ptx::named_barrier_sync(xbar, 128);
       return xflags[buf * 4 + 0] | xflags[buf * 4 + 1] | xflags[buf * 4 + 2] | xflags[buf * 4 + 3];
@@ -815,12 +818,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (!local_abort) {
           const uint32_t s_col = sl ? kSCol1 : kSCol0;
 #pragma unroll
-          for (int c = 0; c < NC; c += 16) {
-            float v16[16];
-            ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + s_col + c0 + c, v16);
+          for (int c = 0; c < NC; c += CW) {
+            float v16[CW];
+            ptx::tmem_ld_32x32b<CW>(tmem_base + lane_addr + s_col + c0 + c, v16);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[c + i] = v16[i];
+            for (int i = 0; i < CW; ++i) x[c + i] = v16[i];
           }
         } else {
 #pragma unroll
@@ -885,14 +888,14 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
             for (int h2 = 0; h2 < Cfg::kOWidth / NPAD; ++h2) {
 #pragma unroll
-              for (int c = 0; c < NC; c += 16) {
+              for (int c = 0; c < NC; c += CW) {
                 const uint32_t col = kOCol + static_cast<uint32_t>(h2 * NPAD + c0 + c);
-                float o16[16];
-                ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + col, o16);
+                float o16[CW];
+                ptx::tmem_ld_32x32b<CW>(tmem_base + lane_addr + col, o16);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o16[i] *= alpha[c + i];
-                ptx::tmem_st_32x32b_x16(tmem_base + lane_addr + col, o16);
+                for (int i = 0; i < CW; ++i) o16[i] *= alpha[c + i];
+                ptx::tmem_st_32x32b<CW>(tmem_base + lane_addr + col, o16);
               }
             }
             ptx::tmem_wait_st();
@@ -972,12 +975,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
       for (int h2 = 0; h2 < kHalves; ++h2) {
 #pragma unroll
-        for (int c = 0; c < NC; c += 16) {
-          float o16[16];
-          ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + kOCol + static_cast<uint32_t>(h2 * NPAD + c0 + c), o16);
+        for (int c = 0; c < NC; c += CW) {
+          float o16[CW];
+          ptx::tmem_ld_32x32b<CW>(tmem_base + lane_addr + kOCol + static_cast<uint32_t>(h2 * NPAD + c0 + c), o16);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[h2 * NC + c + i] = o16[i];
+          for (int i = 0; i < CW; ++i) o[h2 * NC + c + i] = o16[i];
         }
       }
       ptx::tc_fence_before();

@@ -234,6 +234,26 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&v)[16
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The same for 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// W (8 or 16) consecutive columns.
+template <int W>
+__device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, float (&v)[W]) {
+  static_assert(W == 8 || W == 16, "8 or 16 columns");
+  if constexpr (W == 16) tmem_ld_32x32b_x16(taddr, v);
+  else tmem_ld_32x32b_x8(taddr, v);
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -245,6 +265,21 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const float (
         "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
         "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+                 "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+                 "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
+template <int W>
+__device__ __forceinline__ void tmem_st_32x32b(uint32_t taddr, const float (&v)[W]) {
+  static_assert(W == 8 || W == 16, "8 or 16 columns");
+  if constexpr (W == 16) tmem_st_32x32b_x16(taddr, v);
+  else tmem_st_32x32b_x8(taddr, v);
 }
 
 // ------------------------------------------------------- UMMA descriptors
