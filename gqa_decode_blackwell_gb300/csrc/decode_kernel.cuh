@@ -128,13 +128,15 @@ struct DecodeCfg {
   static constexpr int kQBytes = kChunks * NPAD * 128;       // one Q buffer
   static constexpr int kPBytes = 2 * NPAD * 128;             // one P buffer (two 64-position atoms)
   static constexpr int kOWidth = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // TMEM columns of O
-  // Softmax warpgroups.  With 32 columns the softmax is the slower side of
-  // the pipeline, and four warpgroups each take 8 of the columns (their own
-  // running max and sums, their own O columns and rows of P), so that four
-  // times as many warps hide its latencies (measured on GB300: faster than
-  // two warpgroups of 16 columns, which were faster than one).  Warps:
-  // producer, score-MMA issuer, value-MMA issuer, then 4 * kWGs softmax warps.
-  static constexpr int kWGs = NPAD == 32 ? 4 : 1;
+  // Softmax warpgroups, 8 columns each: every warpgroup keeps the running
+  // max and sums, the O columns and the P rows of its own columns, so that
+  // more warps hide the softmax's latencies.  With 32 columns the softmax is
+  // the slower side of the pipeline in steady state; with 16 its per-item
+  // work (first block, epilogue) still sits on the critical path.  Measured
+  // on GB300: four warpgroups beat two of 16 columns, and two beat one of 16.
+  // Warps: producer, score-MMA issuer, value-MMA issuer, then 4 * kWGs
+  // softmax warps.
+  static constexpr int kWGs = NPAD / 8;
   static constexpr int kNC = NPAD / kWGs;  // columns per softmax warpgroup
   static constexpr int kThreads = 96 + 128 * kWGs;
   // fixed part of shared memory after the ring
@@ -457,12 +459,13 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   const int32_t* lens_raw = lens_in_smem ? s_len : p.seqlens;
 
   // Who issues an item's output copies.  Issuing a bulk copy can wait behind
-  // the SM's queued TMA loads for hundreds of cycles.  With 32 columns the
-  // softmax warpgroup is the bottleneck, and the value-MMA thread (idle while
-  // the softmax warpgroup finishes an item) issues them.  With 16 columns the
-  // KV stream is the bottleneck and the first softmax thread issues them
-  // itself: measured on GB300, that build's softmax loop runs faster.
-  constexpr bool kPvStores = (NPAD == 32);
+  // the SM's queued TMA loads for hundreds of cycles.  With several softmax
+  // warpgroups (32 columns) the softmax is the bottleneck, and the value-MMA
+  // thread (idle while the softmax finishes an item) issues them once every
+  // warpgroup has staged its columns.  With one warpgroup (16 columns) the KV
+  // stream is the bottleneck and the first softmax thread issues them itself:
+  // measured on GB300, that build's softmax loop runs faster.
+  constexpr bool kPvStores = (NWG > 1);
 
   // Writes item wi's rows from staging buffer ob with bulk copies: nq copies
   // of G contiguous rows (the G query heads of one token) for O, the same for
