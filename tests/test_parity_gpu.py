@@ -90,8 +90,12 @@ def _nan_tail_inputs(lens, s_max, nq, Hq, Hkv, d, seed, dtype=torch.bfloat16):
     return q, k, v, torch.tensor(lens, dtype=torch.int32)
 
 
+# head columns nq * G: 2, 4, 8 and 12 (16-column kernels: the second 8-column
+# softmax warpgroup partly or wholly padding), 16, 18 and 20 (32-column
+# kernels whose last warpgroup holds only padding) and 32
 EDGE = [(64, 4, 1, False), (64, 8, 4, True), (128, 4, 1, False), (128, 8, 1, False), (128, 8, 4, True),
-        (128, 16, 2, True), (64, 2, 1, False)]
+        (128, 16, 2, True), (64, 2, 1, False), (128, 12, 1, False), (128, 16, 1, False), (64, 5, 4, True),
+        (64, 6, 3, True)]
 
 
 @pytest.mark.parametrize("d,G,nq,causal", EDGE, ids=[f"d{a}-G{b}-nq{c}-{'c' if e else 'n'}" for a, b, c, e in EDGE])
