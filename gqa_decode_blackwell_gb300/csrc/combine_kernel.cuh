@@ -69,10 +69,13 @@ gqa_combine_kernel(const CombineParams p) {
   int n = p.num_splits;
   const int32_t* rec = nullptr;
   if (p.n_pieces != nullptr) {
-    const long long bt = row / p.Hq;  // b * nq + t
-    const int hq = static_cast<int>(row % p.Hq);
-    const long long b = bt / p.nq;
-    rec = p.n_pieces + (b * p.kv_heads + hq / p.G) * 4;  // one 16-byte record per pair
+    // rows < 2^31 with piece counts (at most 512 sequences): 32-bit
+    // divisions, not the emulated 64-bit ones
+    const uint32_t r32 = static_cast<uint32_t>(row);
+    const uint32_t bt = r32 / static_cast<uint32_t>(p.Hq);  // b * nq + t
+    const uint32_t hq = r32 - bt * static_cast<uint32_t>(p.Hq);
+    const uint32_t b = bt / static_cast<uint32_t>(p.nq);
+    rec = p.n_pieces + (static_cast<long long>(b) * p.kv_heads + hq / static_cast<uint32_t>(p.G)) * 4;  // one 16-byte record per pair
   }
   constexpr int kSpec = 4;
   float l0, l1, spec[kSpec][VEC];
