@@ -144,6 +144,14 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Prefetches a 4-D tile into L2: no shared memory, no barrier, no data
+// returned to the issuing thread.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // Bulk (non-tensor) async copy shared -> global, tracked by the issuing
 // thread's bulk async-groups.  Both addresses 16-byte aligned, size a
 // multiple of 16.
