@@ -99,6 +99,9 @@ constexpr int kSoftmaxThread0 = 96;  // first thread of the (first) softmax warp
 constexpr int kMaxSmemB = 512;       // sequences whose lengths are staged in shared memory
 constexpr int kMaxListItems = 128;   // work items of one CTA kept as a list in shared memory
 constexpr float kRescaleThreshold = 8.0f;
+// -max of a column whose max is still -inf: larger than any scaled score can
+// make up for, so a visible score votes for a rescale (which replaces it)
+constexpr float kNoMax = 1.2676506e30f;  // 2^100
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kSCol0 = 0, kSCol1 = 32, kOCol = 64;
 
@@ -846,9 +849,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         continue;
       }
       const int L = it.L;
-      float m[NC], l[NC];  // this warpgroup's columns c0 + n
+      // this warpgroup's columns c0 + n: running max (scaled, log2 units),
+      // per-lane denominator, and -max as the addend of the scaled scores
+      // (kNoMax while the max is -inf: any visible score then votes)
+      float m[NC], l[NC], nms[NC];
 #pragma unroll
-      for (int n = 0; n < NC; ++n) { m[n] = -INFINITY; l[n] = 0.f; }
+      for (int n = 0; n < NC; ++n) { m[n] = -INFINITY; l[n] = 0.f; nms[n] = kNoMax; }
 
       for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
         const bool first = (blk == it.blk_begin);
@@ -880,20 +886,33 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_LD, g);
 
         // ---- mask: position pos is visible to column n when pos < L and,
-        // with the causal mask, n / G >= pos - (L - nq)  (bottom-right)
-        const int pos = blk * kBlockN + r;
-        int n_min = 0;
-        if (p.causal) {
-          const int ahead = pos - (L - p.nq);
-          n_min = ahead > 0 ? ahead * p.G : 0;
+        // with the causal mask, n / G >= pos - (L - nq)  (bottom-right).
+        // Blocks whose rows are all visible to every column skip it; their
+        // padding columns (n >= nq*G, zero query rows) stay unmasked, which
+        // only feeds O columns that are never written out.
+        const bool interior = (blk + 1) * kBlockN <= L - (p.causal ? p.nq - 1 : 0);
+        if (!interior) {
+          const int pos = blk * kBlockN + r;
+          int n_min = 0;
+          if (p.causal) {
+            const int ahead = pos - (L - p.nq);
+            n_min = ahead > 0 ? ahead * p.G : 0;
+          }
+          const bool row_valid = pos < L;
+#pragma unroll
+          for (int n = 0; n < NC; ++n) {
+            const bool vis = row_valid && c0 + n >= n_min && c0 + n < nv;
+            x[n] = vis ? x[n] : -INFINITY;
+          }
         }
-        const bool row_valid = pos < L;
+        // t = scaled score - running max, in log2 units: one FFMA per score
+        // feeds both the rescale vote and the exponent
+        float t[NC];
         bool need = false;
 #pragma unroll
         for (int n = 0; n < NC; ++n) {
-          const bool vis = row_valid && c0 + n >= n_min && c0 + n < nv;
-          x[n] = vis ? x[n] * p.scale_log2 : -INFINITY;
-          need |= x[n] > m[n] + kRescaleThreshold;
+          t[n] = fmaf(x[n], p.scale_log2, nms[n]);
+          need |= t[n] > kRescaleThreshold;
         }
         // An item's first block always takes the max below (m is -inf; with
         // every score masked it leaves m = -inf and l = 0, as skipping it
@@ -917,14 +936,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           const uint32_t f2 = exchange(local_abort ? 2u : 0u, true, wmax);
           if (f2 & 2u) { aborted = true; break; }
           float alpha[NC], bmax[NC];
-          xcombine(bmax, true);
+          xcombine(bmax, true);  // of the unscaled scores: the scale is positive
 #pragma unroll
           for (int n = 0; n < NC; ++n) {
-            const float mn = fmaxf(m[n], bmax[n]);
+            const float mn = fmaxf(m[n], bmax[n] * p.scale_log2);
             const float ms = mn == -INFINITY ? 0.f : mn;
             alpha[n] = ptx::ex2_approx(m[n] - ms);
             m[n] = mn;
             l[n] *= alpha[n];
+            nms[n] = mn == -INFINITY ? kNoMax : -mn;
+            t[n] = fmaf(x[n], p.scale_log2, nms[n]);
           }
           if (!first) {
             // this warpgroup's O columns: c0 + [0, NC), and for head_dim 64
@@ -951,8 +972,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         float pr[NC];
 #pragma unroll
         for (int n = 0; n < NC; ++n) {
-          const float ms = m[n] == -INFINITY ? 0.f : m[n];
-          pr[n] = ptx::ex2_approx(x[n] - ms);
+          pr[n] = ptx::ex2_approx(t[n]);
           l[n] += pr[n];
         }
         // P buffer sl is free once PV(g-2) has completed
