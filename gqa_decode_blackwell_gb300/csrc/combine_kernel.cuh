@@ -14,6 +14,12 @@
 // consecutive output elements, read as one 16- or 8-byte vector per split.
 // Up to 64 splits the LSEs stay in two registers per lane; more splits (a
 // long sequence cut over many CTAs) take a two-pass loop over groups of 32.
+//
+// Four warps per CTA at <= 48 registers a thread (6 K registers) fit beside a
+// resident decode CTA (11 warps at 160 registers, or 19 at 96), so the merge's
+// CTAs are placed while the decode kernel still runs.  The merge releases the
+// next launch in the stream at once: that launch's own grid-dependency wait
+// still covers every output written here.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -23,7 +29,7 @@
 
 namespace gqa {
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 128;
 
 struct CombineParams {
   const float* o_part;      // [num_splits, rows, d]
@@ -53,10 +59,13 @@ __device__ __forceinline__ void load_vec(const float* src, float (&v)[VEC]) {
 }  // namespace detail
 
 template <int HEAD_DIM>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineThreads, 10)
 gqa_combine_kernel(const CombineParams p) {
   constexpr int VEC = HEAD_DIM / 32;  // elements per lane
   constexpr float kLog2e = 1.4426950408889634f;
+  // The next launch may start its set-up now; it waits for this grid to
+  // complete before it reads or writes anything this grid touches.
+  ptx::griddep_launch_dependents();
   // Partials come from the preceding decode launch.
   ptx::griddep_wait();
 
@@ -203,7 +212,6 @@ gqa_combine_kernel(const CombineParams p) {
     else *reinterpret_cast<uint32_t*>(dst) = w[0];
   }
   if (lane == 0 && p.lse != nullptr) p.lse[row] = lse_out;
-  ptx::griddep_launch_dependents();
 }
 
 }  // namespace gqa

@@ -419,33 +419,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     if (lane == 0) ptx::mbar_arrive(BAR(PRE_READY));  // lengths and prefix sums staged
     prod_it.init_warp(plan, lens_in_smem ? s_len : p.seqlens, s_len, s_pre, blockIdx.x, lane);
   } else {
-    if (warp == 1) {
-      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-      ptx::tmem_relinquish();
-    }
-    // Padding rows of Q (beyond nq*G) and both P buffers start at zero; TMA
-    // never writes them.
-    const int nv = p.nq * p.G;
-    const int tid = threadIdx.x - 32;
-    for (int i = tid; i < 2 * KCH * NPAD; i += kThreads - 32) {
-      const int row = i % NPAD;
-      if (row < nv) continue;
-      uint4* dst = reinterpret_cast<uint4*>(qbuf + (i / NPAD) * NPAD * 128 + row * 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-    }
-    uint4* pz = reinterpret_cast<uint4*>(pbuf);
-    for (int i = tid; i < 2 * Cfg::kPBytes / 16; i += kThreads - 32) pz[i] = make_uint4(0, 0, 0, 0);
-    ptx::fence_proxy_async_smem();
-    // Outputs and workspace may still be read by the previous kernel.
-    ptx::griddep_wait();
     if (NPAD == 16 && threadIdx.x == kSoftmaxThread0) {
-      // This CTA's first tiles are prefetched into L2 while the producer
-      // builds the plan, guessed as if every sequence had max_seqlen
-      // positions (a wrong guess costs a few tiles of bandwidth).  Measured on
-      // GB300: 0.2-1.3 us per call faster for the stream-bound 16-column
-      // kernels; the softmax-bound 32-column kernels gain nothing from earlier
-      // first tiles and lost 0.2 us to the extra TMA work.
+      // This CTA's first tiles are prefetched into L2 before the grid
+      // dependency (while the previous launch finishes) and while the
+      // producer builds the plan, guessed as if every sequence had max_seqlen
+      // positions (a wrong guess costs a few tiles of bandwidth).  A prefetch
+      // returns no data, so it cannot observe a value the previous launch
+      // still writes.  Measured on GB300: 0.2-1.3 us per call faster for the
+      // stream-bound 16-column kernels; the softmax-bound 32-column kernels
+      // gain nothing from earlier first tiles and lost 0.2 us to the extra TMA
+      // work.
       const int nblk = num_blocks(plan.max_seqlen);
       const int H = plan.kv_heads;
       const long long pairs = static_cast<long long>(B) * H;
@@ -477,10 +460,34 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           ptx::tma_prefetch_l2_4d(&p.tm_q, kc * 64, h * p.G, 0, b);
           ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, blk * kBlockN, b);
           ptx::tma_prefetch_l2_4d(&p.tm_v, kc * 64, h, blk * kBlockN, b);
-          if (blk + 1 < nblk) ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, (blk + 1) * kBlockN, b);
+          if (blk + 1 < nblk) {
+            ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, (blk + 1) * kBlockN, b);
+            ptx::tma_prefetch_l2_4d(&p.tm_v, kc * 64, h, (blk + 1) * kBlockN, b);
+          }
+          if (blk + 2 < nblk) ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, (blk + 2) * kBlockN, b);
         }
       }
     }
+    if (warp == 1) {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish();
+    }
+    // Padding rows of Q (beyond nq*G) and both P buffers start at zero; TMA
+    // never writes them.
+    const int nv = p.nq * p.G;
+    const int tid = threadIdx.x - 32;
+    for (int i = tid; i < 2 * KCH * NPAD; i += kThreads - 32) {
+      const int row = i % NPAD;
+      if (row < nv) continue;
+      uint4* dst = reinterpret_cast<uint4*>(qbuf + (i / NPAD) * NPAD * 128 + row * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+    uint4* pz = reinterpret_cast<uint4*>(pbuf);
+    for (int i = tid; i < 2 * Cfg::kPBytes / 16; i += kThreads - 32) pz[i] = make_uint4(0, 0, 0, 0);
+    ptx::fence_proxy_async_smem();
+    // Outputs and workspace may still be read by the previous kernel.
+    ptx::griddep_wait();
     if (warp == 2) {
       if (ptx::mbar_wait_bounded(BAR(PRE_READY), 0, abort_flag, p.timeout_ns)) {
         build_list(lane);
