@@ -87,9 +87,12 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 // event costs a clock read and a store, not a dependent global load.
 #define GQA_TRACE_SETUP() unsigned long long* const gqa_trace_buf_ = ::gqa::g_gqa_trace_buf
 #define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event(gqa_trace_buf_, (ev), (idx))
+#define GQA_TRACE_VALUE(ev, idx, v) \
+  do { if (gqa_trace_buf_ != nullptr) gqa_trace_buf_[(static_cast<size_t>(blockIdx.x) * ::gqa::TR_EVENTS + (ev)) * ::gqa::kTraceBlocks + (idx)] = (v); } while (0)
 #else
 #define GQA_TRACE_SETUP() ((void)0)
 #define GQA_TRACE_EVENT(ev, idx) ((void)(idx))  // index evaluated in both builds
+#define GQA_TRACE_VALUE(ev, idx, v) ((void)0)
 #endif
 
 // output element types (the values of gqa_dtype_t)
@@ -332,6 +335,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     ptx::prefetch_tensormap(&p.tm_k);
     ptx::prefetch_tensormap(&p.tm_v);
   }
+#ifdef GQA_TRACE
+  __shared__ unsigned int trace_warps_done;  // warps that reached the teardown barrier
+  if (threadIdx.x == 0) trace_warps_done = 0;
+#endif
+  // every warp reaches the CTA barriers converged (one arrival per warp)
+  __syncwarp();
   __syncthreads();  // barriers initialised
 
   // This CTA's work items, 32 candidates at a time (one per lane), written to
@@ -464,7 +473,11 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
             ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, (blk + 1) * kBlockN, b);
             ptx::tma_prefetch_l2_4d(&p.tm_v, kc * 64, h, (blk + 1) * kBlockN, b);
           }
-          if (blk + 2 < nblk) ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, (blk + 2) * kBlockN, b);
+          if (blk + 2 < nblk) {
+            ptx::tma_prefetch_l2_4d(&p.tm_v, kc * 64, h, (blk + 2) * kBlockN, b);
+            ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, (blk + 2) * kBlockN, b);
+          }
+          if (blk + 3 < nblk) ptx::tma_prefetch_l2_4d(&p.tm_k, kc * 64, h, (blk + 3) * kBlockN, b);
         }
       }
     }
@@ -1117,9 +1130,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   }
 
   // ---------------------------------------------------------------- teardown
+#ifdef GQA_TRACE
+  if (lane == 0) atomicAdd(&trace_warps_done, 1u);
+#endif
   ptx::tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x == 0) GQA_TRACE_EVENT(TR_END, 0);
+  __syncwarp();
+  __syncthreads();  // every role is done with TMEM and shared memory
+  if (threadIdx.x == 0) {
+    GQA_TRACE_EVENT(TR_END, 0);
+    GQA_TRACE_VALUE(TR_END, 1, trace_warps_done);
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
