@@ -130,11 +130,14 @@ int auto_splits(long long pairs, int nblk, int rows_per_pair, int head_dim, int 
   return best_s;
 }
 
-// Item units X of the balanced plan: a work item's fixed cost in blocks.
-// Per-CTA traces on GB300 put a CTA's time at about a + b * blocks + c * items
-// with c / b = 1.5 (16 query columns) to 2.5 (32); timing X = 0..3 on the
-// Llama-shaped, speculative and ragged workloads, X = 3 was best or tied on each.
-constexpr int kItemUnits = 3;
+// Item units X of the balanced plan: a work item's fixed cost in blocks, by
+// the kernel's column count.  Per-CTA traces on GB300 put a CTA's time at
+// about a + b * blocks + c * items with c / b ~1.5 (16 query columns) to ~2
+// (32).  Timed on GB300 (per call): 16 columns, X = 1 / 2 / 3: Llama-8B
+// shape 25.78 / 25.89 / 25.93 us, ragged 137.52 / 137.68 / 137.58 us;
+// 32 columns (speculative shape): 17.97 / 17.60 / 17.60 us.
+constexpr int kItemUnits16 = 1;
+constexpr int kItemUnits32 = 3;
 
 HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_partial) {
   HostPlan hp;
@@ -146,14 +149,26 @@ HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_parti
   const int nblk_cap = num_blocks(d->max_seqlen);
   const long long pairs = static_cast<long long>(d->batch) * d->kv_heads;
   const int rows_per_pair = d->q_tokens * (d->q_heads / d->kv_heads);
+  const int item_units = rows_per_pair <= 16 ? kItemUnits16 : kItemUnits32;
   // the balanced plan keeps per-sequence unit prefix sums in int32
-  const bool pre_fits = static_cast<long long>(d->batch) * pair_units(nblk_cap, kItemUnits) <= 0x7fffffffLL;
+  const bool pre_fits = static_cast<long long>(d->batch) * pair_units(nblk_cap, item_units) <= 0x7fffffffLL;
   if (num_splits == 0 && d->batch <= kMaxSmemB && pre_fits) {
     pp.mode = PLAN_BALANCED;
-    pp.item_units = kItemUnits;
+    // Short sequences with room for k >= 2 CTAs per (batch, KV head) pair
+    // (at most 32 blocks per CTA): the grid is k CTAs per pair and items cost
+    // no units, so equal lengths give every CTA one item of the same size and
+    // every pair k pieces (unequal lengths are still cut into equal ranges).
+    // Measured on GB300 against all SMs with X item units: Llama-8B shape
+    // 25.80 -> 25.18 us per call, speculative 17.71 -> 17.45 us.  Longer
+    // sequences keep every SM: the ragged long-context workload measured
+    // 137.5 us on 152 CTAs and 139.4 us on 128.
+    const long long per_pair = pairs > 0 ? sm / pairs : 0;
+    const bool whole = per_pair >= 2 && nblk_cap <= 32 * per_pair;
+    const long long ctas = whole ? per_pair * pairs : sm;
+    pp.item_units = whole ? 0 : item_units;
     long long units_cap = pairs * pair_units(nblk_cap, pp.item_units);
     if (units_cap < 1) units_cap = 1;
-    pp.num_ctas = static_cast<int>(units_cap < sm ? units_cap : sm);
+    pp.num_ctas = static_cast<int>(units_cap < ctas ? units_cap : ctas);
     pp.num_splits = 0;
     pp.min_blocks = 1;
     const int slots = pp.num_ctas < nblk_cap ? pp.num_ctas : nblk_cap;

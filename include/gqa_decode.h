@@ -213,7 +213,9 @@ const char* gqa_status_string(gqa_status_t status);
  * SMs to plan for (0 = those of the current device; needs no GPU otherwise).  Fills
  * *num_ctas with the grid size, *plan_mode with 0 (fixed splits per sequence)
  * or 1 (balanced contiguous ranges; each non-empty (b, h) pair counts its
- * 128-position blocks plus 3 units for the item's fixed cost) and *num_slots
+ * 128-position blocks plus X units for the item's fixed cost: X = 0 with a
+ * grid of k CTAs per pair when k >= 2 fit on the SMs and S_max spans at most
+ * 32 k blocks, else every SM and X = 1 for nq * G <= 16, 3 above) and *num_slots
  * with the partial slots per row (0 when no combine runs).  If `items` is not NULL, writes up to
  * max_items records of 8 int32 each -- cta, b, h, blk_begin, blk_end, slot
  * (-1 = final output), first_piece, n_pieces -- in the order each CTA

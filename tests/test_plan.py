@@ -29,15 +29,27 @@ def _units(nblk, X):
     return nblk + X if nblk > 0 else 0
 
 
-def check_balanced(seqlens, Hkv, s_max, sm, X=3):
+# Grid and item units X of the balanced plan: with k >= 2 SMs per (batch, KV
+# head) pair and at most 32 blocks per CTA (cache capacity <= 32 k blocks),
+# k CTAs per pair and X = 0; otherwise every SM, and X = 1 for the 16-column
+# kernels (nq * G <= 16), 3 for the 32-column ones.
+def _grid_and_item_units(pairs, sm, G, nq, s_max):
+    k = sm // pairs if pairs > 0 else 0
+    if k >= 2 and _blocks(s_max) <= 32 * k:
+        return k * pairs, 0
+    return sm, (1 if nq * G <= 16 else 3)
+
+
+def check_balanced(seqlens, Hkv, s_max, sm, G=4, nq=1):
     """Balanced plan: every pair costs its blocks plus X item units; the
     units, in pair order (batch-major), are cut into C contiguous ranges."""
-    desc = _desc(len(seqlens), Hkv, s_max)
+    grid, X = _grid_and_item_units(len(seqlens) * Hkv, sm, G, nq, s_max)
+    desc = _desc(len(seqlens), Hkv, s_max, G=G, nq=nq)
     C, mode, slots, items = g.gqa_decode_plan(desc, seqlens, 0, sm)
     assert mode == 1
     lens = [min(max(int(L), 0), s_max) for L in seqlens]
     U = sum(_units(_blocks(L), X) for L in lens) * Hkv
-    assert C == max(1, min(sm, len(lens) * Hkv * _units(_blocks(s_max), X)))
+    assert C == max(1, min(grid, len(lens) * Hkv * _units(_blocks(s_max), X)))
     C_eff = max(1, min(C, U))
 
     def cta_of(u):  # the largest c with floor(c * U / C_eff) <= u
@@ -88,8 +100,9 @@ def check_balanced(seqlens, Hkv, s_max, sm, X=3):
         assert sum(per_cta.values()) == U - X * Hkv * sum(1 for L in lens if L > 0)
 
 
+@pytest.mark.parametrize("G,nq", [(4, 1), (8, 4)])
 @pytest.mark.parametrize("seed", range(24))
-def test_balanced_plan_random(seed):
+def test_balanced_plan_random(seed, G, nq):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 40))
     Hkv = int(rng.choice([1, 2, 8]))
@@ -97,27 +110,47 @@ def test_balanced_plan_random(seed):
     lens = rng.integers(-5, s_max + 1, size=B)
     lens[rng.random(B) < 0.2] = 0
     sm = int(rng.choice([1, 3, 16, 152]))
-    check_balanced(lens.tolist(), Hkv, s_max, sm)
+    check_balanced(lens.tolist(), Hkv, s_max, sm, G, nq)
     # the same lengths in a much larger cache: fewer units than CTAs
-    check_balanced(lens.tolist(), Hkv, s_max * 7, 152)
+    check_balanced(lens.tolist(), Hkv, s_max * 7, 152, G, nq)
 
 
-@pytest.mark.parametrize("lens,Hkv,s_max,sm", [
-    ([0, 0, 0], 2, 128, 152),         # nothing to read: every pair is an empty item
-    ([200], 2, 4200, 152),            # fewer units than CTAs, pairs cut in two
-    ([129], 1, 4200, 152),
-    ([1, 127, 128, 129, 4097, 0, 1], 2, 4200, 152),
-    ([5000, 0, 3], 1, 5000, 16),
-    ([1], 1, 1, 152),                 # one unit, one CTA
-    ([512], 1, 512, 152),             # tiny config: 4 units
-    ([4096] * 8, 8, 4096, 152),       # Llama-8B-shaped
-    ([8192] * 16, 8, 8192, 152),      # 70B-shaped
-    ([2048] * 32, 2, 2048, 152),      # speculative
-    ([131072, 1024, 70000, 0], 8, 131072, 152),
-    ([0, 300, 0, 0, 129, 0], 3, 300, 5),
+@pytest.mark.parametrize("lens,Hkv,s_max,sm,G,nq", [
+    ([0, 0, 0], 2, 128, 152, 4, 1),         # nothing to read: every pair is an empty item
+    ([200], 2, 4200, 152, 4, 1),            # fewer units than CTAs, pairs cut in two
+    ([129], 1, 4200, 152, 4, 1),
+    ([1, 127, 128, 129, 4097, 0, 1], 2, 4200, 152, 4, 1),
+    ([5000, 0, 3], 1, 5000, 16, 4, 1),
+    ([1], 1, 1, 152, 4, 1),                 # one unit, one CTA
+    ([512], 1, 512, 152, 4, 1),             # tiny config: 4 units
+    ([4096] * 8, 8, 4096, 152, 4, 1),       # Llama-8B-shaped
+    ([8192] * 16, 8, 8192, 152, 8, 1),      # 70B-shaped
+    ([2048] * 32, 2, 2048, 152, 8, 4),      # speculative: 32 columns
+    ([131072, 1024, 70000, 0], 8, 131072, 152, 4, 1),
+    ([0, 300, 0, 0, 129, 0], 3, 300, 5, 4, 1),
 ])
-def test_balanced_plan_cases(lens, Hkv, s_max, sm):
-    check_balanced(lens, Hkv, s_max, sm)
+def test_balanced_plan_cases(lens, Hkv, s_max, sm, G, nq):
+    check_balanced(lens, Hkv, s_max, sm, G, nq)
+
+
+@pytest.mark.parametrize("B,Hkv,L,G,nq,ctas,pieces", [
+    (8, 8, 4096, 4, 1, 128, 2),     # Llama-8B-shaped: 64 pairs, two CTAs each
+    (32, 2, 2048, 8, 4, 128, 2),    # speculative
+    (4, 8, 8192, 8, 1, 128, 4),     # 32 pairs, four CTAs each
+    (16, 8, 8192, 8, 1, 152, None), # 128 pairs on 152 SMs: every SM
+    (4, 8, 131072, 8, 1, 152, None),  # long sequences: every SM
+])
+def test_balanced_plan_equal_lengths_one_item_per_cta(B, Hkv, L, G, nq, ctas, pieces):
+    """Equal lengths with two or more SMs per pair: every CTA gets one item of
+    the same size, every pair the same number of pieces."""
+    C, mode, slots, items = g.gqa_decode_plan(_desc(B, Hkv, L, G=G, nq=nq), [L] * B, 0, 152)
+    assert mode == 1 and C == ctas
+    if pieces is not None:
+        per_cta = collections.Counter(int(r[0]) for r in items)
+        assert len(per_cta) == ctas and set(per_cta.values()) == {1}
+        assert {int(r[4]) - int(r[3]) for r in items} == {(L // 128) // pieces}
+        assert {int(r[7]) for r in items} == {pieces}
+    check_balanced([L] * B, Hkv, L, 152, G, nq)
 
 
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 64])
