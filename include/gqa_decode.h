@@ -25,9 +25,12 @@
  * Conventions shared by every call:
  *   - Pointers are device pointers unless stated otherwise; the caller owns
  *     all memory.  The library never allocates, frees or memsets device
- *     memory.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream) and contain no host synchronisation, so they can
- *     be captured in a CUDA graph.
+ *     memory (gqa_decode_attn_static_workspace uses a static array).  Calls
+ *     are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and contain no host synchronisation.  gqa_decode_attn and
+ *     gqa_decode_attn_split are captured in CUDA graphs and replayed in this
+ *     library's tests and benchmark, after one call outside capture (the
+ *     first call on a device sets kernel attributes); do the same.
  *   - Tensors are dense, row-major, in the layouts stated per argument.
  *   - Arguments are checked before anything is launched; an invalid call
  *     returns an error status and launches nothing.
