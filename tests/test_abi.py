@@ -105,3 +105,39 @@ def test_selftest_argument_checks(L):
 def test_workspace_size_of_invalid_description_is_zero(L):
     assert L.gqa_decode_workspace_size(ctypes.byref(_desc(head_dim=96)), 0) == 0
     assert L.gqa_decode_workspace_size(None, 0) == 0
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """A C99 translation unit that includes the header and calls every
+    declared function compiles warning-free and links against the library."""
+    import os
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    calls = {
+        "gqa_decode_workspace_size": "(void)gqa_decode_workspace_size(&d, 0);",
+        "gqa_decode_attn": "(void)gqa_decode_attn(&d, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0);",
+        "gqa_decode_attn_static_workspace": "(void)gqa_decode_attn_static_workspace(&d, 0, 0, 0, 0, 0, 0, 0, 0);",
+        "gqa_decode_attn_split": "(void)gqa_decode_attn_split(&d, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0);",
+        "gqa_decode_attn_merge": "(void)gqa_decode_attn_merge(&d, 0, 0, 0, 0, 0, 0);",
+        "gqa_decode_splitkv": "(void)gqa_decode_splitkv(&d, 0, 0, 0, 0, 1, 0, 0, 0);",
+        "gqa_decode_combine": "(void)gqa_decode_combine(0, 0, 1, 0, 64, 0, GQA_DTYPE_FP32, 0, 0);",
+        "gqa_decode_get_error": "(void)gqa_decode_get_error(0);",
+        "gqa_status_string": "(void)gqa_status_string(GQA_OK);",
+        "gqa_decode_plan": "(void)gqa_decode_plan(&d, 0, 0, 1, &n, &m, &s, 0, 0, &ni);",
+        "gqa_decode_selftest_timeout": "(void)gqa_decode_selftest_timeout(0u, 0);",
+    }
+    assert set(calls) == set(g.header_functions())
+    src = tmp_path / "use.c"
+    src.write_text('#include "gqa_decode.h"\n'
+                   "int main(void) {\n"
+                   "  gqa_desc_t d = {0};\n  int n = 0, m = 0, s = 0;\n  int64_t ni = 0;\n"
+                   + "".join(f"  {c}\n" for c in calls.values()) +
+                   "  (void)n; (void)m; (void)s; (void)ni;\n  return 0;\n}\n")
+    lib = gbuild.LIB
+    exe = tmp_path / "use"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                    os.path.join(gbuild.ROOT, "include"), str(src), lib, "-o", str(exe)], check=True)
