@@ -4,10 +4,18 @@
 A step is one gqa_decode_attn call (split-KV decode kernel + LSE combine)
 over one batch of seeded synthetic input already resident in HBM.  Steps
 cycle through a rotating pool of distinct KV caches larger than L2 and are
-replayed from CUDA graphs of back-to-back calls.  Defaults: the Llama-8B
-shaped workload (B8, 32/8 heads, d128, L4096, bf16), automatic splitting,
-one GPU.  With torchrun, every rank runs an independent replica (the work
-does not shard with an exchange step) and the slowest rank's time is used.
+replayed from CUDA graphs of back-to-back calls.  Defaults: the long-context
+ragged workload (B4, 64/8 heads, d128, lengths uniform in [1024, 131072],
+bf16; the largest of the five workloads), automatic splitting, one GPU.
+With torchrun, every rank runs an independent replica (the work does not
+shard with an exchange step) and the slowest rank's time is used.
+
+Timing: `value` is the mean over the K timed steps (one CUDA-event pair
+around them).  Beside it, `pages_method` repeats the measurement the way
+"Building a Faster GQA Decode Kernel for Blackwell SM100" ("Performance
+against FA4") times its kernels: the fastest of 3 round medians, 7 graph
+replays per round, rounds of the full call and of the decode kernel alone
+interleaved.
 
 --impl reference times the fp64 CPU oracle on the host cores instead.
 """
@@ -211,6 +219,28 @@ class GraphSteps:
         if rem:
             self._graph(rem).replay()
 
+    def replay_times_ms(self, replays: int, stream):
+        """Per-call times of `replays` replays of the pool graph, each timed
+        with its own CUDA-event pair on `stream`."""
+        gf = self._graph(self.per)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+        for a, b in evs:
+            a.record(stream)
+            gf.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) / self.per for a, b in evs]
+
+
+def pages_method(steps: GraphSteps, dec_steps: GraphSteps, stream, rounds: int = 3, replays: int = 7):
+    """Fastest of `rounds` round medians of `replays` timed graph replays,
+    rounds of the full call and of the decode kernel alone interleaved."""
+    call, dec = [], []
+    for _ in range(rounds):
+        call.append(statistics.median(steps.replay_times_ms(replays, stream)))
+        dec.append(statistics.median(dec_steps.replay_times_ms(replays, stream)))
+    return min(call), min(dec)
+
 
 def bench_ours(args, cfg, world, rank, local):
     import gqa_decode_blackwell_gb300 as g
@@ -222,6 +252,10 @@ def bench_ours(args, cfg, world, rank, local):
     splits = args.splits
     in_dtype = torch.float16 if args.dtype == "fp16" else torch.bfloat16
     out_dtype = torch.float32 if cfg.out_dtype == "fp32" else in_dtype
+    if args.len_div > 1:
+        cfg = workloads.shrink(cfg, seqlen=max(1, cfg.seqlen // args.len_div),
+                               ragged=None if cfg.ragged is None else
+                               tuple(max(1, x // args.len_div) for x in cfg.ragged))
     host = workloads.make_inputs(cfg, dtype=in_dtype)
     kv_bytes = host.kv_bytes()
     alloc_bytes = host.k_cache.numel() * 2 * 2
@@ -291,6 +325,7 @@ def bench_ours(args, cfg, world, rank, local):
     e1.record(cur)
     torch.cuda.synchronize()
     ms_decode = e0.elapsed_time(e1) / dec_n
+    pm_call, pm_dec = pages_method(steps, dec_steps, cur)
     if clocks:
         clocks.stop()
     if g.gqa_decode_get_error(clear=True) != g.GQA_OK:
@@ -330,7 +365,10 @@ def bench_ours(args, cfg, world, rank, local):
 
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (ms_decode * 1e-3) / 1e9
-    traffic, traffic_src = ncu_traffic(cfg.name)
+    if args.len_div == 1:
+        traffic, traffic_src = ncu_traffic(cfg.name)
+    else:
+        traffic, traffic_src = None, "lengths divided for a profiling capture"
     roofline = {"bound": "hbm", "kernel": "gqa_decode_kernel", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": traffic, "traffic_source": traffic_src, "us_per_launch": round(ms_decode * 1e3, 3),
@@ -349,11 +387,17 @@ def bench_ours(args, cfg, world, rank, local):
                    "q_tokens": cfg.q_tokens, "q_heads": cfg.q_heads, "kv_heads": cfg.kv_heads,
                    "head_dim": cfg.head_dim, "seqlen": cfg.seqlen if cfg.ragged is None else "ragged",
                    "seqlens_sum": int(host.seqlens.sum().item()), "kv_bytes_per_step": kv_bytes,
+                   "len_div": args.len_div,
                    "num_splits": "auto" if splits == 0 else splits, "plan": ["splits", "balanced"][mode],
                    "ctas": nc, "partial_slots": slots,
                    "l2": f"rotating pool of {pool} KV caches ({pool * alloc_bytes / 1e6:.0f} MB) > 129 MB L2",
                    "launch": f"CUDA graphs of {pool} back-to-back calls, PDL between kernels",
                    "parallelism": f"replicas x{world}"},
+        "pages_method": {"us_per_call": round(pm_call * 1e3, 3), "decode_kernel_us": round(pm_dec * 1e3, 3),
+                         "gbs": round(kv_bytes / (pm_call * 1e-3) / 1e9, 2),
+                         "frac_of_peak": round(kv_bytes / (pm_call * 1e-3) / 1e9 / peak, 4),
+                         "how": "fastest of 3 round medians, 7 graph replays of the pool per round, "
+                                "full-call and decode-only rounds interleaved"},
         "roofline": roofline, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary() if clocks else None, "e2e": e2e, "cpu_baseline": cpu,
     }
@@ -418,7 +462,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="llama8b", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="ragged", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--len-div", type=int, default=1,
+                    help="divide the workload's KV lengths by this (smaller profiling captures only)")
     ap.add_argument("--splits", type=int, default=None, help="0 = automatic (default: the config's first)")
     ap.add_argument("--pool-mb", type=float, default=512.0)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16", help="element type of q, k and v")

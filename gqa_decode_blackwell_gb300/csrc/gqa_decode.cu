@@ -492,7 +492,9 @@ gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const voi
   if (num_splits < 1 || num_splits > GQA_MAX_SPLITS) return GQA_ERR_INVALID_ARG;
   if (desc->batch == 0) return GQA_OK;
   if ((rc = check_inputs(q, k_cache, v_cache, seqlens)) != GQA_OK) return rc;
-  if (o_part == nullptr || lse_part == nullptr || !aligned(o_part, 16) || !aligned(lse_part, 4))
+  // Both partial buffers must be 16-byte aligned: the kernel writes their
+  // rows with bulk async copies, which need 16-byte aligned addresses.
+  if (o_part == nullptr || lse_part == nullptr || !aligned(o_part, 16) || !aligned(lse_part, 16))
     return GQA_ERR_INVALID_ARG;
   int dev = 0;
   DeviceState* st = nullptr;

@@ -136,10 +136,15 @@ gqa_status_t gqa_decode_attn(const gqa_desc_t* desc, const void* q, const void* 
  * with GQA_ERR_WORKSPACE before anything is launched.  The call allocates and
  * frees nothing.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Every call on a device shares the one
- * array and nothing in it needs clearing (each call writes every value it
- * reads), but calls whose kernels overlap on the GPU -- on different streams,
- * or different host threads -- race on it: order them on one stream.
+ * call before any stream capture.  The address is kept for the life of the
+ * process: resetting a device (cudaDeviceReset) while this library is loaded
+ * is not supported.  Every call on a device shares the one array, which
+ * keeps the last call's contents, and nothing in it needs clearing: the
+ * merge may load slots this call did not write (the partials of empty
+ * splits), but their weight is exactly zero (lse = -inf, or a piece count
+ * that excludes them), so they never affect the result.  Calls whose kernels
+ * overlap on the GPU -- on different streams, or different host threads --
+ * race on the array: order them on one stream.
  */
 #define GQA_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
 gqa_status_t gqa_decode_attn_static_workspace(const gqa_desc_t* desc, const void* q,
@@ -171,9 +176,11 @@ gqa_status_t gqa_decode_attn_merge(const gqa_desc_t* desc, void* out, float* lse
  * nblk = ceil(L_b / 128).  Writes the normalised partial output and its LSE
  * of every split:
  *   o_part    fp32 [num_splits, B, nq, Hq, d], 16-byte aligned
- *   lse_part  fp32 [num_splits, B, nq, Hq]; lse_part = -inf marks an empty
- *             split (s >= splits_b, or no visible key), whose o_part entries
- *             are left unwritten (gqa_decode_combine ignores them)
+ *   lse_part  fp32 [num_splits, B, nq, Hq], 16-byte aligned (its rows leave
+ *             by bulk async copies; any other address is GQA_ERR_INVALID_ARG
+ *             before launch); lse_part = -inf marks an empty split
+ *             (s >= splits_b, or no visible key), whose o_part entries are
+ *             left unwritten (gqa_decode_combine ignores them)
  * num_splits: 1..64.  gqa_decode_combine merges the result.
  */
 gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const void* k_cache,
@@ -204,6 +211,10 @@ gqa_status_t gqa_decode_combine(const float* o_part, const float* lse_part, int 
  * out (the kernel then returned early and its outputs are invalid),
  * GQA_ERR_BAD_SEQLEN if a length was clamped, GQA_OK otherwise.  Synchronises
  * with the device (call it after the work of interest has finished).
+ * After GQA_ERR_TIMEOUT from a decode kernel, treat the CUDA context as
+ * suspect: the kernel's own clean-up waits are bounded too, so asynchronous
+ * copies or MMAs it had issued may still have been in flight when it
+ * returned.  Rebuild the context before relying on it again.
  */
 gqa_status_t gqa_decode_get_error(int clear);
 

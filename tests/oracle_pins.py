@@ -296,6 +296,70 @@ def pin_split_then_combine(orc):
             assert np.allclose(lse[fin], full_lse[fin], atol=1e-12, rtol=0)
 
 
+# Key ranges of the documented split partition, worked out by hand from its
+# definition (the one gqa_decode_splitkv states): sequence b of length L has
+# nblk = ceil(L / block) blocks and splits = clamp(ceil(nblk / min_blocks), 1, S)
+# splits; split s < splits covers blocks [floor(s*nblk/splits),
+# floor((s+1)*nblk/splits)), i.e. positions [128*lo, min(128*hi, L)), and the
+# splits past `splits` are empty ([0, 0)).  Entries: (L, S, min_blocks, block)
+# -> [(begin, end) of split 0, 1, ..., S-1].
+SPLIT_TABLE = [
+    ((0, 1, 1, 128), [(0, 0)]),
+    ((0, 3, 1, 128), [(0, 0), (0, 0), (0, 0)]),
+    ((1, 1, 1, 128), [(0, 1)]),
+    ((1, 3, 1, 128), [(0, 1), (0, 0), (0, 0)]),
+    ((128, 3, 1, 128), [(0, 128), (0, 0), (0, 0)]),
+    ((129, 1, 1, 128), [(0, 129)]),
+    ((129, 3, 1, 128), [(0, 128), (128, 129), (0, 0)]),
+    ((129, 8, 1, 128), [(0, 128), (128, 129)] + [(0, 0)] * 6),
+    ((1000, 1, 1, 128), [(0, 1000)]),
+    # nblk = 8 over 3 splits: floor(8/3) = 2, floor(16/3) = 5
+    ((1000, 3, 1, 128), [(0, 256), (256, 640), (640, 1000)]),
+    ((1000, 8, 1, 128), [(128 * s, 128 * (s + 1)) for s in range(7)] + [(896, 1000)]),
+    # at least 3 blocks a split: ceil(8/3) = 3 splits even when 8 are allowed
+    ((1000, 8, 3, 128), [(0, 256), (256, 640), (640, 1000)] + [(0, 0)] * 5),
+    ((129, 8, 3, 128), [(0, 129)] + [(0, 0)] * 7),
+    # 4-position blocks: L = 10 has 3 blocks, floor(3/2) = 1
+    ((10, 2, 1, 4), [(0, 4), (4, 10)]),
+    ((10, 5, 1, 4), [(0, 4), (4, 8), (8, 10), (0, 0), (0, 0)]),
+]
+
+
+def pin_split_ranges(orc, split_ranges=None):
+    """The oracle's split partition (oracle.split_ranges) against the table
+    above, worked by hand from the partition's definition, one sequence at a
+    time and all of them in one batch; plus the properties any reading of it
+    must have: the non-empty ranges are contiguous, block-aligned, cover
+    [0, L) exactly and number min(S, ceil(nblk / min_blocks)) (at least 1)."""
+    fn = oracle_mod.split_ranges if split_ranges is None else split_ranges
+    for (L, S, mb, blk), want in SPLIT_TABLE:
+        begin, end = fn([L], S, block=blk, min_blocks=mb)
+        got = [(int(begin[s, 0]), int(end[s, 0])) for s in range(S)]
+        assert got == want, ((L, S, mb, blk), got, want)
+    # a batch gives each sequence its own partition
+    for S, mb, blk in ((3, 1, 128), (8, 1, 128), (8, 3, 128)):
+        rows = [(key, want) for key, want in SPLIT_TABLE if key[1:] == (S, mb, blk)]
+        lens = [key[0] for key, _ in rows]
+        begin, end = fn(lens, S, block=blk, min_blocks=mb)
+        for i, (_, want) in enumerate(rows):
+            assert [(int(begin[s, i]), int(end[s, i])) for s in range(S)] == want
+    # properties on a sweep
+    for L in list(range(0, 600, 7)) + [1023, 1024, 1025, 131072]:
+        for S in (1, 2, 3, 4, 5, 8, 16, 64):
+            nblk = -(-L // 128)
+            begin, end = fn([L], S)
+            ranges = [(int(begin[s, 0]), int(end[s, 0])) for s in range(S)]
+            n_live = min(S, max(nblk, 1))
+            live, dead = ranges[:n_live], ranges[n_live:]
+            assert all(r == (0, 0) for r in dead), (L, S, ranges)
+            assert live[0][0] == 0 and live[-1][1] == L, (L, S, ranges)
+            for (b0, e0), (b1, _) in zip(live, live[1:]):
+                assert e0 == b1 and b1 % 128 == 0, (L, S, ranges)
+            sizes = [-(-(e - b) // 128) for b, e in live]
+            if L > 0:
+                assert max(sizes) - min(sizes) <= 1 and min(sizes) >= 1, (L, S, ranges)
+
+
 def pin_lse_logsumexp(orc):
     """The LSE at moderate sizes (several hundred keys, ragged and empty rows,
     both mask modes) against scipy's logsumexp of fp64 scores from a numpy
@@ -359,6 +423,7 @@ ALL_PINS = [
     pin_shift_and_scale_invariance,
     pin_head_map_golden,
     pin_split_then_combine,
+    pin_split_ranges,
     pin_lse_logsumexp,
     pin_combine_closed_forms,
 ]

@@ -81,6 +81,19 @@ def test_bad_split_counts(L):
     assert rc == g.GQA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("G", [4, 8, 3])
+def test_splitkv_rejects_lse_part_off_16_bytes(L, G):
+    """The kernel writes lse_part rows with bulk async copies (16-byte
+    aligned addresses only), so a 4- or 8-byte aligned lse_part is refused
+    before anything is launched -- for every group size, including those
+    whose rows would be 16-byte multiples."""
+    d = _desc(q_heads=2 * G, kv_heads=2)
+    for off in (4, 8, 12):
+        rc = L.gqa_decode_splitkv(ctypes.byref(d), ALIGNED, ALIGNED, ALIGNED, ALIGNED, 2, ALIGNED, ALIGNED + off,
+                                  None)
+        assert rc == g.GQA_ERR_INVALID_ARG, off
+
+
 def test_empty_batch_is_a_no_op(L):
     assert _attn(L, _desc(batch=0)) == g.GQA_OK
 
