@@ -265,19 +265,24 @@ def bench_ours(args, cfg, world, rank, local):
                                               base.seqlens.clone(), base.scale) for _ in range(pool - 1)]
     out = torch.empty(base.q.shape, dtype=out_dtype, device=dev)
     lse = torch.empty(base.q.shape[:3], dtype=torch.float32, device=dev)
-    ws_bytes = g.gqa_decode_workspace_size(base.q, base.k_cache, splits, causal=cfg.causal, out_dtype=out_dtype)
+    red = args.reduction
+    ws_bytes = g.gqa_decode_workspace_size(base.q, base.k_cache, splits, causal=cfg.causal, out_dtype=out_dtype,
+                                           reduction=red)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    nc, mode, slots, _ = g.gqa_decode_plan(g.make_desc(base.q, base.k_cache, causal=cfg.causal, out_dtype=out_dtype),
+    nc, mode, slots, _ = g.gqa_decode_plan(g.make_desc(base.q, base.k_cache, causal=cfg.causal, out_dtype=out_dtype,
+                                                       reduction=red),
                                            host.seqlens.tolist(), splits, 0, max_items=1)
     launches_per_step = 1 + (1 if slots > 0 else 0)
 
     def attn(j):
         c = copies[j % pool]
-        g.gqa_decode_attn(c.q, c.k_cache, c.v_cache, c.seqlens, out, lse, splits, ws, causal=cfg.causal)
+        g.gqa_decode_attn(c.q, c.k_cache, c.v_cache, c.seqlens, out, lse, splits, ws, causal=cfg.causal,
+                          reduction=red)
 
     def split_only(j):
         c = copies[j % pool]
-        g.gqa_decode_attn_split(c.q, c.k_cache, c.v_cache, c.seqlens, out, lse, splits, ws, causal=cfg.causal)
+        g.gqa_decode_attn_split(c.q, c.k_cache, c.v_cache, c.seqlens, out, lse, splits, ws, causal=cfg.causal,
+                                reduction=red)
 
     stream = torch.cuda.Stream(device=dev)
     for j in range(pool):  # eager once per copy: kernel attributes, tensor maps
@@ -331,6 +336,33 @@ def bench_ours(args, cfg, world, rank, local):
     if g.gqa_decode_get_error(clear=True) != g.GQA_OK:
         raise RuntimeError("decode reported a device error in the timed region")
 
+    # Eager calls (no graph): host time per C-ABI call, measured on the
+    # ctypes call with its arguments prepared once (argument checks, plan,
+    # tensor maps, launches), and the device time per call of the same run.
+    import ctypes
+
+    lib = g.lib()
+    desc = g.make_desc(base.q, base.k_cache, causal=cfg.causal, out_dtype=out_dtype, reduction=red)
+    argsets = [(ctypes.byref(desc), c.q.data_ptr(), c.k_cache.data_ptr(), c.v_cache.data_ptr(),
+                c.seqlens.data_ptr(), out.data_ptr(), lse.data_ptr(), splits, ws.data_ptr(),
+                ws.numel(), cur.cuda_stream) for c in copies]
+    n_eager = 200
+    for j in range(2 * pool):
+        lib.gqa_decode_attn(*argsets[j % pool])
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    q0.record(cur)
+    for j in range(n_eager):
+        lib.gqa_decode_attn(*argsets[j % pool])
+    host_us = (time.perf_counter() - h0) * 1e6 / n_eager
+    q1.record(cur)
+    torch.cuda.synchronize()
+    eager = {"host_us_per_call": round(host_us, 3), "us_per_call": round(q0.elapsed_time(q1) * 1e3 / n_eager, 3),
+             "calls": n_eager}
+    if g.gqa_decode_get_error(clear=True) != g.GQA_OK:
+        raise RuntimeError("decode reported a device error in the eager calls")
+
     # end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -344,7 +376,7 @@ def bench_ours(args, cfg, world, rank, local):
         def e2e_step():
             for dst, src in zip(d, h):
                 dst.copy_(src, non_blocking=True)
-            g.gqa_decode_attn(d[0], d[1], d[2], d[3], out, lse, splits, ws, causal=cfg.causal)
+            g.gqa_decode_attn(d[0], d[1], d[2], d[3], out, lse, splits, ws, causal=cfg.causal, reduction=red)
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -388,7 +420,8 @@ def bench_ours(args, cfg, world, rank, local):
                    "head_dim": cfg.head_dim, "seqlen": cfg.seqlen if cfg.ragged is None else "ragged",
                    "seqlens_sum": int(host.seqlens.sum().item()), "kv_bytes_per_step": kv_bytes,
                    "len_div": args.len_div,
-                   "num_splits": "auto" if splits == 0 else splits, "plan": ["splits", "balanced"][mode],
+                   "num_splits": "auto" if splits == 0 else splits,
+                   "plan": ["splits", "balanced", "splits merged in clusters"][mode], "reduction": red,
                    "ctas": nc, "partial_slots": slots,
                    "l2": f"rotating pool of {pool} KV caches ({pool * alloc_bytes / 1e6:.0f} MB) > 129 MB L2",
                    "launch": f"CUDA graphs of {pool} back-to-back calls, PDL between kernels",
@@ -398,6 +431,7 @@ def bench_ours(args, cfg, world, rank, local):
                          "frac_of_peak": round(kv_bytes / (pm_call * 1e-3) / 1e9 / peak, 4),
                          "how": "fastest of 3 round medians, 7 graph replays of the pool per round, "
                                 "full-call and decode-only rounds interleaved"},
+        "eager": eager,
         "roofline": roofline, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary() if clocks else None, "e2e": e2e, "cpu_baseline": cpu,
     }
@@ -468,6 +502,8 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=None, help="0 = automatic (default: the config's first)")
     ap.add_argument("--pool-mb", type=float, default=512.0)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16", help="element type of q, k and v")
+    ap.add_argument("--reduction", choices=["auto", "combine", "cluster"], default="auto",
+                    help="how split partials are merged (auto: the library's selection)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")

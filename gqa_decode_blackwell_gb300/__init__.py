@@ -27,6 +27,10 @@ GQA_ERR_BAD_SEQLEN = 6
 GQA_DTYPE_BF16 = 0
 GQA_DTYPE_FP32 = 1
 GQA_DTYPE_FP16 = 2
+GQA_REDUCE_AUTO = 0
+GQA_REDUCE_COMBINE = 1
+GQA_REDUCE_CLUSTER = 2
+_REDUCTIONS = {"auto": GQA_REDUCE_AUTO, "combine": GQA_REDUCE_COMBINE, "cluster": GQA_REDUCE_CLUSTER}
 
 _lock = threading.Lock()
 _lib = None
@@ -50,6 +54,7 @@ class gqa_desc_t(ctypes.Structure):
         ("causal", ctypes.c_int),
         ("out_dtype", ctypes.c_int),
         ("in_dtype", ctypes.c_int),
+        ("reduction", ctypes.c_int),
     ]
 
 
@@ -125,9 +130,19 @@ def _dtype_code(dtype, allowed):
     return code
 
 
-def make_desc(q, k_cache, *, scale: float = 0.0, causal: bool = False, out_dtype=None) -> gqa_desc_t:
+def _reduction_code(reduction) -> int:
+    if isinstance(reduction, str):
+        if reduction not in _REDUCTIONS:
+            raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}")
+        return _REDUCTIONS[reduction]
+    return int(reduction)
+
+
+def make_desc(q, k_cache, *, scale: float = 0.0, causal: bool = False, out_dtype=None,
+              reduction="auto") -> gqa_desc_t:
     """Problem description from q [B, nq, Hq, d] and a cache [B, S_max, Hkv, d]
-    (inputs bf16 or fp16; out_dtype fp32 or the inputs' type, the default)."""
+    (inputs bf16 or fp16; out_dtype fp32 or the inputs' type, the default;
+    reduction "auto", "combine" or "cluster", see gqa_reduction_t)."""
     import torch
 
     B, nq, Hq, d = q.shape
@@ -138,7 +153,8 @@ def make_desc(q, k_cache, *, scale: float = 0.0, causal: bool = False, out_dtype
         out_dtype = q.dtype
     code = _dtype_code(out_dtype, (GQA_DTYPE_BF16, GQA_DTYPE_FP32, GQA_DTYPE_FP16))
     in_code = _dtype_code(q.dtype, (GQA_DTYPE_BF16, GQA_DTYPE_FP16))
-    return gqa_desc_t(B, nq, Hq, Hkv, d, s_max, float(scale), int(bool(causal)), code, in_code)
+    return gqa_desc_t(B, nq, Hq, Hkv, d, s_max, float(scale), int(bool(causal)), code, in_code,
+                      _reduction_code(reduction))
 
 
 def _inputs_ok(q, k_cache, v_cache, seqlens):
@@ -153,16 +169,17 @@ def _inputs_ok(q, k_cache, v_cache, seqlens):
         raise ValueError("seqlens must be a contiguous int32 tensor")
 
 
-def gqa_decode_workspace_size(q, k_cache, num_splits: int = 0, *, causal: bool = False, out_dtype=None) -> int:
-    desc = make_desc(q, k_cache, causal=causal, out_dtype=out_dtype)
+def gqa_decode_workspace_size(q, k_cache, num_splits: int = 0, *, causal: bool = False, out_dtype=None,
+                              reduction="auto") -> int:
+    desc = make_desc(q, k_cache, causal=causal, out_dtype=out_dtype, reduction=reduction)
     return int(lib().gqa_decode_workspace_size(ctypes.byref(desc), int(num_splits)))
 
 
 def gqa_decode_attn(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int = 0, workspace=None, *,
-                    scale: float = 0.0, causal: bool = False, stream=None) -> None:
+                    scale: float = 0.0, causal: bool = False, reduction="auto", stream=None) -> None:
     """Full decode into ``out`` (and ``lse``); see gqa_decode_attn in the C header."""
     _inputs_ok(q, k_cache, v_cache, seqlens)
-    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype)
+    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype, reduction=reduction)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().gqa_decode_attn(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
                                _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), ws_bytes, _stream(stream))
@@ -170,11 +187,12 @@ def gqa_decode_attn(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int
 
 
 def gqa_decode_attn_static_workspace(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int = 0, *,
-                                     scale: float = 0.0, causal: bool = False, stream=None) -> None:
+                                     scale: float = 0.0, causal: bool = False, reduction="auto",
+                                     stream=None) -> None:
     """gqa_decode_attn using the library's static device workspace instead of a
     caller-allocated one (for callers that cannot allocate; see the C header)."""
     _inputs_ok(q, k_cache, v_cache, seqlens)
-    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype)
+    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype, reduction=reduction)
     rc = lib().gqa_decode_attn_static_workspace(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                                 _ptr(seqlens), _ptr(out), _ptr(lse), int(num_splits),
                                                 _stream(stream))
@@ -182,10 +200,10 @@ def gqa_decode_attn_static_workspace(q, k_cache, v_cache, seqlens, out, lse=None
 
 
 def gqa_decode_attn_split(q, k_cache, v_cache, seqlens, out, lse=None, num_splits: int = 0, workspace=None, *,
-                          scale: float = 0.0, causal: bool = False, stream=None) -> None:
+                          scale: float = 0.0, causal: bool = False, reduction="auto", stream=None) -> None:
     """The decode-kernel half of gqa_decode_attn (see the C header)."""
     _inputs_ok(q, k_cache, v_cache, seqlens)
-    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype)
+    desc = make_desc(q, k_cache, scale=scale, causal=causal, out_dtype=out.dtype, reduction=reduction)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().gqa_decode_attn_split(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens),
                                      _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), ws_bytes,
@@ -194,9 +212,9 @@ def gqa_decode_attn_split(q, k_cache, v_cache, seqlens, out, lse=None, num_split
 
 
 def gqa_decode_attn_merge(q, k_cache, out, lse=None, num_splits: int = 0, workspace=None, *, causal: bool = False,
-                          stream=None) -> None:
+                          reduction="auto", stream=None) -> None:
     """The combine half of gqa_decode_attn over the workspace of gqa_decode_attn_split."""
-    desc = make_desc(q, k_cache, causal=causal, out_dtype=out.dtype)
+    desc = make_desc(q, k_cache, causal=causal, out_dtype=out.dtype, reduction=reduction)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().gqa_decode_attn_merge(ctypes.byref(desc), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace),
                                      ws_bytes, _stream(stream))
@@ -260,7 +278,7 @@ def gqa_decode_selftest_timeout(timeout_us: int, stream=None) -> None:
 
 
 def decode(q, k_cache, v_cache, seqlens, *, num_splits: int = 0, scale: float = 0.0, causal: bool = False,
-           out_dtype=None, stream=None):
+           out_dtype=None, reduction="auto", stream=None):
     """Allocates out / lse / workspace with torch and calls gqa_decode_attn."""
     import torch
 
@@ -268,8 +286,9 @@ def decode(q, k_cache, v_cache, seqlens, *, num_splits: int = 0, scale: float = 
     B, nq, Hq, d = q.shape
     out = torch.empty(B, nq, Hq, d, dtype=out_dtype, device=q.device)
     lse = torch.empty(B, nq, Hq, dtype=torch.float32, device=q.device)
-    ws_bytes = gqa_decode_workspace_size(q, k_cache, num_splits, causal=causal, out_dtype=out_dtype)
+    ws_bytes = gqa_decode_workspace_size(q, k_cache, num_splits, causal=causal, out_dtype=out_dtype,
+                                         reduction=reduction)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device) if ws_bytes else None
     gqa_decode_attn(q, k_cache, v_cache, seqlens, out, lse, num_splits, ws, scale=scale, causal=causal,
-                    stream=stream)
+                    reduction=reduction, stream=stream)
     return out, lse

@@ -10,8 +10,8 @@
 // so the output is bit-identical from run to run, and the maximum is taken here
 // from the staged lse values (no global running-max buffer, nothing to reset).
 //
-// One warp per row; each lane owns 4 (head_dim 128) or 2 (head_dim 64)
-// consecutive output elements, read as one 16- or 8-byte vector per split.
+// One warp per row; each lane owns 8 (head_dim 256), 4 (128) or 2 (64)
+// consecutive output elements, read as 32-, 16- or 8-byte vectors per split.
 // Up to 64 splits the LSEs stay in two registers per lane; more splits (a
 // long sequence cut over many CTAs) take a two-pass loop over groups of 32.
 //
@@ -47,7 +47,12 @@ namespace detail {
 
 template <int VEC>
 __device__ __forceinline__ void load_vec(const float* src, float (&v)[VEC]) {
-  if constexpr (VEC == 4) {
+  if constexpr (VEC == 8) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+    const float4 y = __ldg(reinterpret_cast<const float4*>(src) + 1);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+  } else if constexpr (VEC == 4) {
     const float4 x = __ldg(reinterpret_cast<const float4*>(src));
     v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
   } else {
@@ -192,8 +197,14 @@ gqa_combine_kernel(const CombineParams p) {
 
   if (p.out_dtype == 1) {  // fp32
     float* dst = static_cast<float*>(p.out) + row * HEAD_DIM + lane * VEC;
-    if constexpr (VEC == 4) *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    else *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+    if constexpr (VEC == 8) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else if constexpr (VEC == 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    } else {
+      *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+    }
   } else {
     // two 16-bit values per 32-bit word, bf16 or fp16
     uint32_t w[VEC / 2];
@@ -208,7 +219,8 @@ gqa_combine_kernel(const CombineParams p) {
       }
     }
     uint16_t* dst = static_cast<uint16_t*>(p.out) + row * HEAD_DIM + lane * VEC;
-    if constexpr (VEC == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    if constexpr (VEC == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    else if constexpr (VEC == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
     else *reinterpret_cast<uint32_t*>(dst) = w[0];
   }
   if (lane == 0 && p.lse != nullptr) p.lse[row] = lse_out;

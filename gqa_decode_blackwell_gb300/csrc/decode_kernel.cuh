@@ -106,6 +106,7 @@ constexpr float kRescaleThreshold = 8.0f;
 // make up for, so a visible score votes for a rescale (which replaces it)
 constexpr float kNoMax = 1.2676506e30f;  // 2^100
 constexpr uint32_t kTmemCols = 128;
+constexpr int kMaxClusterK = 8;  // CTAs of an in-cluster merge: a power of two, the portable cluster size
 constexpr uint32_t kSCol0 = 0, kSCol1 = 32, kOCol = 64;
 
 struct DecodeParams {
@@ -124,16 +125,31 @@ struct DecodeParams {
   int causal;
   float scale_log2;   // softmax scale * log2(e)
   int lse_bulk;       // LSE rows may be written by 16-byte bulk copies (G % 4 == 0, aligned)
+  int cluster_k;      // > 1: the CTAs of a k-cluster hold the k pieces of a pair and merge them in
+                      // distributed shared memory (fixed splits, k = plan.num_splits)
   unsigned long long timeout_ns;
 };
 
 template <int HEAD_DIM, int NPAD>
 struct DecodeCfg {
   static constexpr int kChunks = HEAD_DIM / 64;            // 128-byte swizzle atoms along d
-  static constexpr int kSlotBytes = kBlockN * HEAD_DIM * 2;  // one K or V block
+  // A ring tile holds 128 positions x at most 128 elements of d: head_dim 256
+  // streams each K or V block as two d-halves (two tiles), so that the ring
+  // keeps 32 KB stages.  S^T accumulates over both K halves; O^T is two
+  // M = 128 accumulators, one per V half.
+  static constexpr int kTileDim = HEAD_DIM < 128 ? HEAD_DIM : 128;
+  static constexpr int kTileChunks = kTileDim / 64;
+  static constexpr int kTilesPerBlock = HEAD_DIM / kTileDim;
+  static constexpr int kSlotBytes = kBlockN * kTileDim * 2;  // one K or V tile
   static constexpr int kQBytes = kChunks * NPAD * 128;       // one Q buffer
   static constexpr int kPBytes = 2 * NPAD * 128;             // one P buffer (two 64-position atoms)
-  static constexpr int kOWidth = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // TMEM columns of O
+  // TMEM columns of O: head_dim 64 stacks two position halves, 256 has two d-halves
+  static constexpr int kOWidth = HEAD_DIM == 128 ? NPAD : 2 * NPAD;
+  static constexpr int kPvN = HEAD_DIM == 64 ? 2 * NPAD : NPAD;  // N of one value MMA
+  // Q and output staging buffers: two each (the next item's Q loads, and the
+  // previous item's rows leave, while this item runs); one each where two do
+  // not fit beside a 4-stage ring (head_dim 256 with 32 columns)
+  static constexpr int kBufs = (HEAD_DIM == 256 && NPAD == 32) ? 1 : 2;
   // Softmax warpgroups, 8 columns each: every warpgroup keeps the running
   // max and sums, the O columns and the P rows of its own columns, so that
   // more warps hide the softmax's latencies.  With 32 columns the softmax is
@@ -157,7 +173,11 @@ struct DecodeCfg {
   // output staging, two buffers: one item's rows (fp32 worst case), its LSEs,
   // its piece count
   static constexpr int kOutBytes = (NPAD * HEAD_DIM * 4 + 128 + 16 + 127) / 128 * 128;
-  static constexpr int kFixedBytes = 2 * kQBytes + 2 * kPBytes + kMiscBytes + 2 * kOutBytes + kXoBytes;
+  // in-cluster merge: this CTA's merged columns of an item (at most half of
+  // d, fp32, per row), then the merged LSEs
+  static constexpr int kFinBytes = (NPAD * HEAD_DIM * 2 + NPAD * 4 + 127) / 128 * 128;
+  static constexpr int kFixedBytes =
+      kBufs * kQBytes + 2 * kPBytes + kMiscBytes + kBufs * kOutBytes + kXoBytes + kFinBytes;
   static constexpr int kSmemBudget = 227 * 1024 - 1024;  // minus alignment slack
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kSlotBytes;
   // Four stages (two K, two V blocks) per SM keep enough bytes in flight
@@ -177,7 +197,9 @@ struct DecodeCfg {
   static_assert(kStages >= 4 && kStagesV >= 2, "ring too shallow");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory over budget");
   static_assert(kOWidth <= 64 && NPAD <= 32, "TMEM column plan");
-  static_assert(kMiscBytes % 128 == 0 && (2 * kQBytes + 2 * kPBytes) % 128 == 0, "staging alignment");
+  static_assert(kMiscBytes % 128 == 0 && (kBufs * kQBytes + 2 * kPBytes) % 128 == 0, "staging alignment");
+  // K and V rings of whole blocks' tiles
+  static_assert(kStagesK % kTilesPerBlock == 0 && kStagesV % kTilesPerBlock == 0, "ring of whole blocks");
 };
 
 namespace detail {
@@ -268,8 +290,11 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* qbuf = ring + Cfg::kRingBytes;                // 2 x kQBytes
-  uint8_t* pbuf = qbuf + 2 * Cfg::kQBytes;               // 2 x kPBytes
+  constexpr uint32_t NB = Cfg::kBufs;                    // Q / output staging buffers
+  constexpr int TPB = Cfg::kTilesPerBlock;               // ring tiles per K or V block
+  constexpr int TCH = Cfg::kTileChunks;                  // 64-element chunks per tile
+  uint8_t* qbuf = ring + Cfg::kRingBytes;                // NB x kQBytes
+  uint8_t* pbuf = qbuf + NB * Cfg::kQBytes;              // 2 x kPBytes
   uint8_t* misc = pbuf + 2 * Cfg::kPBytes;
   uint64_t* bar = reinterpret_cast<uint64_t*>(misc);     // 64 barrier words max
   // per softmax warpgroup: flags [2][4], then values [2][4][NC]
@@ -286,7 +311,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   auto obuf_of = [&](int ob) -> uint8_t* { return misc + Cfg::kMiscBytes + ob * Cfg::kOutBytes; };
   auto lse_of = [&](int ob) -> float* { return reinterpret_cast<float*>(obuf_of(ob) + NPAD * HEAD_DIM * 4); };
   auto np_of = [&](int ob) -> int32_t* { return reinterpret_cast<int32_t*>(lse_of(ob) + 32); };
-  float* xo_buf = reinterpret_cast<float*>(obuf_of(0) + 2 * Cfg::kOutBytes);  // kXoBytes
+  float* xo_buf = reinterpret_cast<float*>(obuf_of(0) + NB * Cfg::kOutBytes);  // kXoBytes
+  uint8_t* fin_buf = obuf_of(0) + NB * Cfg::kOutBytes + Cfg::kXoBytes;         // kFinBytes
+  const bool cluster_merge = p.cluster_k > 1;
 
   // barrier indices
   const uint32_t bar_base = ptx::smem_u32(bar);
@@ -308,6 +335,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // (PLAN_READY), and the rest allocate TMEM and zero the padding of the MMA
   // operand buffers.
   const int PLAN_READY = DRAIN + 2, OUT_FULL = DRAIN + 3, OUT_EMPTY = DRAIN + 5, PRE_READY = DRAIN + 7;
+  // in-cluster merge, per softmax warpgroup and staging buffer: all k CTAs
+  // have staged the warpgroup's rows (PEER_FULL) / have read them (PEER_EMPTY)
+  const int PEER_FULL = DRAIN + 8, PEER_EMPTY = DRAIN + 8 + 2 * NWG;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       ptx::mbar_init(BAR(RING_FULL + i), 1);
@@ -329,6 +359,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ptx::mbar_init(BAR(OUT_FULL + i), NWG);  // each warpgroup's staging done
       ptx::mbar_init(BAR(OUT_EMPTY + i), 1);
     }
+    if (cluster_merge) {
+      for (int i = 0; i < 2 * NWG; ++i) {
+        ptx::mbar_init(BAR(PEER_FULL + i), static_cast<uint32_t>(p.cluster_k));  // one arrival per CTA
+        ptx::mbar_init(BAR(PEER_EMPTY + i), static_cast<uint32_t>(p.cluster_k));
+      }
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&p.tm_q);
@@ -342,6 +378,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // every warp reaches the CTA barriers converged (one arrival per warp)
   __syncwarp();
   __syncthreads();  // barriers initialised
+  // The other CTAs of the cluster arrive on this CTA's barriers: all of them
+  // must be initialised first.  A hardware barrier over straight-line code
+  // (the cluster's CTAs are scheduled together).
+  if (cluster_merge) ptx::cluster_sync_all();
 
   // This CTA's work items, 32 candidates at a time (one per lane), written to
   // the shared list by the 32 lanes of one warp.  Owned items form a
@@ -489,7 +529,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     // never writes them.
     const int nv = p.nq * p.G;
     const int tid = threadIdx.x - 32;
-    for (int i = tid; i < 2 * KCH * NPAD; i += kThreads - 32) {
+    for (int i = tid; i < static_cast<int>(NB) * KCH * NPAD; i += kThreads - 32) {
       const int row = i % NPAD;
       if (row < nv) continue;
       uint4* dst = reinterpret_cast<uint4*>(qbuf + (i / NPAD) * NPAD * 128 + row * 128);
@@ -580,7 +620,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       int kq = 0;       // non-empty items
       bool have_prev = false, ok = true;
       int pb = 0, ph = 0, pblk = 0;
-      auto load_tile = [&](bool is_v, int b, int h, int blk) -> bool {
+      // tile `half` of block blk: d elements [half * kTileDim, (half + 1) * kTileDim)
+      auto load_tile = [&](bool is_v, int b, int h, int blk, int half) -> bool {
         const uint32_t n = is_v ? tv : tk;
         const uint32_t stage = is_v ? NSK + n % NSV : n % NSK;
         const uint32_t phase = (n / (is_v ? NSV : NSK)) & 1u;
@@ -594,9 +635,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         uint8_t* dst = ring + stage * Cfg::kSlotBytes;
         const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
 #pragma unroll
-        for (int kc = 0; kc < KCH; ++kc)
-          ptx::tma_load_4d_hint(ptx::smem_u32(dst + kc * 16384), map, BAR(RING_FULL + stage), kc * 64, h,
-                                blk * kBlockN, b, policy);
+        for (int kc = 0; kc < TCH; ++kc)
+          ptx::tma_load_4d_hint(ptx::smem_u32(dst + kc * 16384), map, BAR(RING_FULL + stage),
+                                (half * TCH + kc) * 64, h, blk * kBlockN, b, policy);
         if (is_v) {
           GQA_TRACE_EVENT(TR_PROD_V, tv);
           ++tv;
@@ -610,8 +651,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       while (ok && prod_it.next(it)) {
         if (it.blk_begin >= it.blk_end) continue;
         GQA_TRACE_EVENT(TR_PROD_PLAN, static_cast<uint32_t>(kq));
-        const int qb = kq & 1;
-        if (kq >= 2 && !ptx::mbar_wait_bounded(BAR(Q_EMPTY + qb), ((kq >> 1) & 1) ^ 1, abort_flag, p.timeout_ns)) {
+        const int qb = static_cast<int>(static_cast<uint32_t>(kq) % NB);
+        if (kq >= static_cast<int>(NB) &&
+            !ptx::mbar_wait_bounded(BAR(Q_EMPTY + qb), ((static_cast<uint32_t>(kq) / NB) & 1u) ^ 1u, abort_flag,
+                                    p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -623,12 +666,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         GQA_TRACE_EVENT(TR_PROD_Q, static_cast<uint32_t>(kq));
         ++kq;
         for (int blk = it.blk_begin; blk < it.blk_end && ok; ++blk) {
-          ok = load_tile(false, it.b, it.h, blk);
-          if (ok && have_prev) ok = load_tile(true, pb, ph, pblk);
+          for (int hf = 0; hf < TPB && ok; ++hf) ok = load_tile(false, it.b, it.h, blk, hf);
+          for (int hf = 0; hf < TPB && ok && have_prev; ++hf) ok = load_tile(true, pb, ph, pblk, hf);
           pb = it.b; ph = it.h; pblk = blk; have_prev = true;
         }
       }
-      if (ok && have_prev) ok = load_tile(true, pb, ph, pblk);
+      for (int hf = 0; hf < TPB && ok && have_prev; ++hf) ok = load_tile(true, pb, ph, pblk, hf);
       if (!ok) {
         detail::set_error(kErrTimeout, abort_flag);
         // let the copies already issued land before the CTA exits
@@ -636,8 +679,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           ptx::mbar_wait_bounded(BAR(RING_FULL + u % NSK), (u / NSK) & 1u, nullptr, p.timeout_ns);
         for (uint32_t u = tv > NSV ? tv - NSV : 0u; u < tv; ++u)
           ptx::mbar_wait_bounded(BAR(RING_FULL + NSK + u % NSV), (u / NSV) & 1u, nullptr, p.timeout_ns);
-        for (int k = (kq > 2 ? kq - 2 : 0); k < kq; ++k)
-          ptx::mbar_wait_bounded(BAR(Q_FULL + (k & 1)), (k >> 1) & 1, nullptr, p.timeout_ns);
+        for (int k = (kq > static_cast<int>(NB) ? kq - static_cast<int>(NB) : 0); k < kq; ++k)
+          ptx::mbar_wait_bounded(BAR(Q_FULL + static_cast<int>(static_cast<uint32_t>(k) % NB)),
+                                 (static_cast<uint32_t>(k) / NB) & 1u, nullptr, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -654,7 +698,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       const bool is_qk = (warp == 1);
       const uint64_t ring_desc = ptx::smem_desc_sw128(ptx::smem_u32(ring), 16, 1024);
       const uint64_t q_desc = ptx::smem_desc_sw128(ptx::smem_u32(qbuf), 16, 1024);
-      const uint64_t v_desc = ptx::smem_desc_sw128(ptx::smem_u32(ring), HEAD_DIM == 128 ? 16384 : 8192, 1024);
+      const uint64_t v_desc =
+          ptx::smem_desc_sw128(ptx::smem_u32(ring), Cfg::kTileDim == 128 ? 16384 : 8192, 1024);
       const uint64_t p_desc = ptx::smem_desc_sw128(ptx::smem_u32(pbuf), 16, 1024);
       constexpr uint32_t kSlot16 = Cfg::kSlotBytes >> 4;  // descriptor units (16 B)
       bool ok = true;
@@ -667,87 +712,109 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         constexpr uint32_t idesc_qk = ptx::idesc_f16_f32(128, NPAD, 0, 0, !IN_F16);
         while (ok && iter.next(it)) {
           if (it.blk_begin >= it.blk_end) continue;
-          const int qb = kq & 1;
-          if (!ptx::mbar_wait_bounded(BAR(Q_FULL + qb), (kq >> 1) & 1, abort_flag, p.timeout_ns)) {
+          const int qb = static_cast<int>(static_cast<uint32_t>(kq) % NB);
+          if (!ptx::mbar_wait_bounded(BAR(Q_FULL + qb), (static_cast<uint32_t>(kq) / NB) & 1u, abort_flag,
+                                      p.timeout_ns)) {
             ok = false;
             break;
           }
           const uint64_t qd = q_desc + static_cast<uint64_t>(qb * (Cfg::kQBytes >> 4));
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
             const uint32_t sl = g & 1u;
-            const uint32_t stage = g % NSK;
-            ok = (g < 2 || ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns)) &&
-                 ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSK) & 1u, abort_flag, p.timeout_ns);
+            ok = g < 2 || ptx::mbar_wait_bounded(BAR(S_EMPTY + sl), ((g >> 1) & 1u) ^ 1u, abort_flag, p.timeout_ns);
             if (!ok) break;
-            GQA_TRACE_EVENT(TR_MMA_K, g);
-            ptx::tc_fence_after();
-            const uint64_t kd = ring_desc + static_cast<uint64_t>(stage * kSlot16);
             const uint32_t d_tmem = tmem_base + (sl ? kSCol1 : kSCol0);
+            // S^T = K Q^T over d, one ring tile (at most 128 elements of d) at a time
 #pragma unroll
-            for (int k = 0; k < HEAD_DIM / 16; ++k) {
-              const uint32_t off_a = static_cast<uint32_t>((k >> 2) * (16384 >> 4) + (k & 3) * 2);
-              const uint32_t off_b = static_cast<uint32_t>((k >> 2) * (NPAD * 128 >> 4) + (k & 3) * 2);
-              ptx::mma_f16_ss(d_tmem, kd + off_a, qd + off_b, idesc_qk, k > 0 ? 1u : 0u);
+            for (int hf = 0; hf < TPB; ++hf) {
+              const uint32_t u = g * TPB + static_cast<uint32_t>(hf);  // K-ring tile
+              const uint32_t stage = u % NSK;
+              ok = ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (u / NSK) & 1u, abort_flag, p.timeout_ns);
+              if (!ok) break;
+              if (hf == 0) GQA_TRACE_EVENT(TR_MMA_K, g);
+              ptx::tc_fence_after();
+              const uint64_t kd = ring_desc + static_cast<uint64_t>(stage * kSlot16);
+#pragma unroll
+              for (int kk = 0; kk < Cfg::kTileDim / 16; ++kk) {
+                const int k = hf * (Cfg::kTileDim / 16) + kk;  // 16-element step of d
+                const uint32_t off_a = static_cast<uint32_t>((kk >> 2) * (16384 >> 4) + (kk & 3) * 2);
+                const uint32_t off_b = static_cast<uint32_t>((k >> 2) * (NPAD * 128 >> 4) + (k & 3) * 2);
+                ptx::mma_f16_ss(d_tmem, kd + off_a, qd + off_b, idesc_qk, k > 0 ? 1u : 0u);
+              }
+              if (hf == TPB - 1) ptx::mma_commit(BAR(S_FULL + sl));
+              ptx::mma_commit(BAR(RING_EMPTY + stage));
             }
-            ptx::mma_commit(BAR(S_FULL + sl));
-            ptx::mma_commit(BAR(RING_EMPTY + stage));
+            if (!ok) break;
             if (blk == it.blk_end - 1) ptx::mma_commit(BAR(Q_EMPTY + qb));
             GQA_TRACE_EVENT(TR_MMA_QK, g);
           }
+          if (!ok) break;
           ++kq;
         }
       } else {
-        constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, Cfg::kOWidth, 1, 0, !IN_F16);
+        constexpr uint32_t idesc_pv = ptx::idesc_f16_f32(128, Cfg::kPvN, 1, 0, !IN_F16);
         uint32_t k = 0;  // items
         while (ok && iter.next(it)) {
           for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
             const uint32_t sl = g & 1u;
-            const uint32_t stage = NSK + g % NSV;
             if (!ptx::mbar_wait_bounded(BAR(P_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns)) {
               ok = false;
               break;
             }
             GQA_TRACE_EVENT(TR_MMA_P, g);
-            if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSV) & 1u, abort_flag, p.timeout_ns)) {
-              ok = false;
-              break;
-            }
-            GQA_TRACE_EVENT(TR_MMA_V, g);
-            ptx::tc_fence_after();
-            const uint64_t vd = v_desc + static_cast<uint64_t>(stage * kSlot16);
             const uint64_t pd = p_desc + static_cast<uint64_t>(sl * (Cfg::kPBytes >> 4));
             const bool first = (blk == it.blk_begin);
-            if constexpr (HEAD_DIM == 128) {
+            // O^T += V^T P^T, one ring tile (d-half) at a time into its own
+            // accumulator (head_dim 256: columns kOCol and kOCol + NPAD)
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const uint32_t off_b = static_cast<uint32_t>((k >> 2) * (NPAD * 128 >> 4) + (k & 3) * 2);
-                ptx::mma_f16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)), pd + off_b,
-                                 idesc_pv, (k > 0 || !first) ? 1u : 0u);
+            for (int hf = 0; hf < TPB; ++hf) {
+              const uint32_t u = g * TPB + static_cast<uint32_t>(hf);  // V-ring tile
+              const uint32_t stage = NSK + u % NSV;
+              if (!ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (u / NSV) & 1u, abort_flag, p.timeout_ns)) {
+                ok = false;
+                break;
               }
-            } else {
+              if (hf == 0) GQA_TRACE_EVENT(TR_MMA_V, g);
+              ptx::tc_fence_after();
+              const uint64_t vd = v_desc + static_cast<uint64_t>(stage * kSlot16);
+              const uint32_t o_tmem = tmem_base + kOCol + static_cast<uint32_t>(hf * NPAD);
+              if constexpr (Cfg::kTileDim == 128) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                ptx::mma_f16_ss(tmem_base + kOCol, vd + static_cast<uint32_t>(k * (2048 >> 4)),
-                                 pd + static_cast<uint32_t>(k * 2), idesc_pv, (k > 0 || !first) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint32_t off_b = static_cast<uint32_t>((kk >> 2) * (NPAD * 128 >> 4) + (kk & 3) * 2);
+                  ptx::mma_f16_ss(o_tmem, vd + static_cast<uint32_t>(kk * (2048 >> 4)), pd + off_b, idesc_pv,
+                                   (kk > 0 || !first) ? 1u : 0u);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  ptx::mma_f16_ss(o_tmem, vd + static_cast<uint32_t>(kk * (2048 >> 4)),
+                                   pd + static_cast<uint32_t>(kk * 2), idesc_pv, (kk > 0 || !first) ? 1u : 0u);
+                }
               }
+              if (hf == TPB - 1) ptx::mma_commit(BAR(P_EMPTY + sl));
+              ptx::mma_commit(BAR(RING_EMPTY + stage));
             }
-            ptx::mma_commit(BAR(P_EMPTY + sl));
-            ptx::mma_commit(BAR(RING_EMPTY + stage));
+            if (!ok) break;
             GQA_TRACE_EVENT(TR_MMA_PV, g);
           }
           if (!ok) break;
-          if constexpr (kPvStores) {
+          if (kPvStores && !cluster_merge) {
             // The softmax warpgroup hands over this item's staged rows before
             // it sends the next item's first P, so nothing is delayed by
-            // waiting here.  Once this item's copies are issued, the previous
-            // item's copies have read their buffer and it can be reused.
-            const int ob = static_cast<int>(k & 1u);
-            if (!ptx::mbar_wait_bounded(BAR(OUT_FULL + ob), (k >> 1) & 1u, abort_flag, p.timeout_ns)) {
+            // waiting here.  With two buffers, once this item's copies are
+            // issued the previous item's copies have read theirs and it can be
+            // reused; with one, this item's copies must have read it.
+            const int ob = static_cast<int>(k % NB);
+            if (!ptx::mbar_wait_bounded(BAR(OUT_FULL + ob), (k / NB) & 1u, abort_flag, p.timeout_ns)) {
               ok = false;
               break;
             }
             store_item(it, ob);
-            if (k >= 1) {
+            if constexpr (NB == 1) {
+              ptx::bulk_wait_read_all();
+              ptx::mbar_arrive(BAR(OUT_EMPTY));
+            } else if (k >= 1) {
               ptx::bulk_wait_read_all_but_last();
               ptx::mbar_arrive(BAR(OUT_EMPTY + (ob ^ 1)));
             }
@@ -824,25 +891,158 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     uint32_t k_out = 0;  // items staged
     auto wait_staging = [&]() -> bool {
       if (threadIdx.x != sm0) return true;
+      if (cluster_merge) {
+        // every CTA of the cluster has read this buffer's rows of the item two before
+        if (k_out < NB) return true;
+        return ptx::mbar_wait_cluster_bounded(BAR(PEER_EMPTY + 2 * wg + static_cast<int>(k_out % NB)),
+                                              ((k_out / NB) & 1u) ^ 1u, abort_flag, p.timeout_ns);
+      }
       if constexpr (!kPvStores) {
         ptx::bulk_wait_read_all();
         return true;
       } else {
-        if (k_out < 2) return true;
-        return ptx::mbar_wait_bounded(BAR(OUT_EMPTY + (k_out & 1u)), ((k_out >> 1) & 1u) ^ 1u, abort_flag,
+        if (k_out < NB) return true;
+        return ptx::mbar_wait_bounded(BAR(OUT_EMPTY + (k_out % NB)), ((k_out / NB) & 1u) ^ 1u, abort_flag,
                                       p.timeout_ns);
       }
     };
+    // In-cluster merge of an item (cluster_k > 1; "Building a Faster GQA
+    // Decode Kernel for Blackwell SM100", section "Reducing inside a thread
+    // block cluster", with a fixed-order sum in place of the page's
+    // reduce-add into a zeroed output).  Every CTA of the cluster has staged
+    // its piece's normalised fp32 rows and LSEs; this warpgroup's rows are
+    // exchanged through distributed shared memory, and CTA j merges columns
+    // [j d/k, (j+1) d/k) of them -- M = max_s lse_s, w_s = exp(lse_s - M),
+    // O = sum_s w_s O_s / sum_s w_s in split order s = 0..k-1, empty pieces
+    // (lse = -inf) skipped -- and writes them out; CTA 0 writes the LSEs.
+    // Returns false on a timeout (uniform over the warpgroup).
+    auto cluster_merge_item = [&](const WorkItem& wi) -> bool {
+      const uint32_t kc = static_cast<uint32_t>(p.cluster_k);
+      const uint32_t crank = ptx::cluster_ctarank();
+      const int ob = static_cast<int>(k_out % NB);
+      const uint32_t full_bar = BAR(PEER_FULL + 2 * wg + ob);
+      const uint32_t empty_bar = BAR(PEER_EMPTY + 2 * wg + ob);
+      ptx::named_barrier_sync(xbar, 128);  // this warpgroup's rows are staged
+      if (threadIdx.x == sm0) {
+        ptx::fence_acq_rel_cluster();
+        for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(full_bar, s2));
+        ptx::bulk_wait_read_all();  // the previous item's output copies have read fin
+      }
+      bool ok = ptx::mbar_wait_cluster_bounded(full_bar, (k_out / NB) & 1u, abort_flag, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (exchange(ok ? 0u : 2u, false, 0.f) & 2u) return false;
+
+      constexpr float kLog2e = 1.4426950408889634f;
+      const int dk = HEAD_DIM / static_cast<int>(kc);  // output columns of this CTA
+      const int ncv = dk >> 2;                         // 4-column groups per row
+      const bool out16 = p.out_dtype != kOutF32;
+      uint8_t* fin_w = fin_buf + wg * (NC * HEAD_DIM * 2);
+      float* fin_lse = reinterpret_cast<float*>(fin_buf + NPAD * HEAD_DIM * 2);
+      // one (row, 4-column group) per thread and pass: NC rows x d / (4k) groups
+      for (int tw = static_cast<int>(threadIdx.x) - sm0; tw < NC * ncv; tw += 128) {
+        const int n = c0 + tw / ncv, cg = tw - (tw / ncv) * ncv;
+        if (n >= nv) continue;
+        const int col = static_cast<int>(crank) * dk + cg * 4;
+        const uint32_t o_loc = ptx::smem_u32(obuf_of(ob)) + static_cast<uint32_t>((n * HEAD_DIM + col) * 4);
+        const uint32_t l_loc = ptx::smem_u32(lse_of(ob) + n);
+        // The LSEs of all pieces first (their maximum), then the weighted
+        // rows two pieces at a time: few registers live at once.
+        float M = -INFINITY;
+#pragma unroll 1
+        for (uint32_t s2 = 0; s2 < kc; ++s2)
+          M = fmaxf(M, ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, s2)));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lse_out = -INFINITY;
+        if (M != -INFINITY) {
+          float W = 0.f;
+#pragma unroll 1
+          for (uint32_t s2 = 0; s2 < kc; s2 += 2) {
+            // kc is a power of two >= 2: pieces s2 and s2 + 1
+            const float la = ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, s2));
+            const float lb = ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, s2 + 1));
+            const float4 oa = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, s2));
+            const float4 o2 = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, s2 + 1));
+            const float wa = la == -INFINITY ? 0.f : ptx::ex2_approx((la - M) * kLog2e);
+            const float wb = lb == -INFINITY ? 0.f : ptx::ex2_approx((lb - M) * kLog2e);
+            W += wa;
+            if (wa != 0.f) {
+              acc.x += wa * oa.x; acc.y += wa * oa.y; acc.z += wa * oa.z; acc.w += wa * oa.w;
+            }
+            W += wb;
+            if (wb != 0.f) {
+              acc.x += wb * o2.x; acc.y += wb * o2.y; acc.z += wb * o2.z; acc.w += wb * o2.w;
+            }
+          }
+          const float inv = 1.0f / W;
+          acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+          lse_out = M + 0.69314718055994531f * __log2f(W);
+        }
+        const int e = (n - c0) * dk + cg * 4;  // element of this warpgroup's merged rows
+        if (out16) {
+          uint32_t w2[2];
+          if constexpr (IN_F16) {
+            __half2 a = __floats2half2_rn(acc.x, acc.y), b2 = __floats2half2_rn(acc.z, acc.w);
+            w2[0] = *reinterpret_cast<uint32_t*>(&a);
+            w2[1] = *reinterpret_cast<uint32_t*>(&b2);
+          } else {
+            __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b2 = __floats2bfloat162_rn(acc.z, acc.w);
+            w2[0] = *reinterpret_cast<uint32_t*>(&a);
+            w2[1] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint2*>(fin_w + e * 2) = make_uint2(w2[0], w2[1]);
+        } else {
+          *reinterpret_cast<float4*>(fin_w + e * 4) = acc;
+        }
+        if (crank == 0 && cg == 0) fin_lse[n] = lse_out;
+      }
+      ptx::fence_proxy_async_smem();       // the merged rows are read by bulk copies
+      ptx::named_barrier_sync(xbar, 128);  // every peer load of this item is done
+      if (threadIdx.x == sm0) {
+        for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(empty_bar, s2));
+        const uint32_t esz = out16 ? 2u : 4u;
+        const uint32_t slice = static_cast<uint32_t>(dk) * esz;
+        const int n_end = c0 + NC < nv ? c0 + NC : nv;
+        for (int n2 = c0; n2 < n_end; ++n2) {
+          const int t = n2 / p.G, g2 = n2 - t * p.G;
+          const long long grow =
+              (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G + g2;
+          ptx::bulk_store(static_cast<uint8_t*>(p.out) + (grow * HEAD_DIM + static_cast<long long>(crank) * dk) * esz,
+                          ptx::smem_u32(fin_w + (n2 - c0) * slice), slice);
+        }
+        if (crank == 0 && p.lse != nullptr) {
+          // runs of rows of one query token are contiguous in lse
+          for (int n2 = c0; n2 < n_end;) {
+            const int t = n2 / p.G;
+            const int run_end = (t + 1) * p.G < n_end ? (t + 1) * p.G : n_end;
+            const long long grow = (static_cast<long long>(wi.b) * p.nq + t) * p.Hq +
+                                   static_cast<long long>(wi.h) * p.G + (n2 - t * p.G);
+            if (p.lse_bulk) {
+              ptx::bulk_store(p.lse + grow, ptx::smem_u32(fin_lse + n2), static_cast<uint32_t>(run_end - n2) * 4u);
+            } else {
+              for (int i = n2; i < run_end; ++i) p.lse[grow + (i - n2)] = fin_lse[i];
+            }
+            n2 = run_end;
+          }
+        }
+        ptx::bulk_commit();
+      }
+      ++k_out;
+      return true;
+    };
+
     // Makes the staged rows visible to the async proxy and writes them out
-    // (or hands them to the value-MMA thread).
-    auto hand_over = [&](const WorkItem& wi) {
+    // (or hands them to the value-MMA thread, or merges them in the cluster).
+    // Returns false on a timeout.
+    auto hand_over = [&](const WorkItem& wi) -> bool {
+      if (cluster_merge) return cluster_merge_item(wi);
       ptx::fence_proxy_async_smem();
       ptx::named_barrier_sync(xbar, 128);
       if (threadIdx.x == sm0) {
-        if constexpr (kPvStores) ptx::mbar_arrive(BAR(OUT_FULL + (k_out & 1u)));
-        else store_item(wi, static_cast<int>(k_out & 1u));
+        if constexpr (kPvStores) ptx::mbar_arrive(BAR(OUT_FULL + (k_out % NB)));
+        else store_item(wi, static_cast<int>(k_out % NB));
       }
       ++k_out;
+      return true;
     };
 
     ItemSource iter;
@@ -855,17 +1055,17 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         // empty item: final output O = 0, lse = -inf; partial lse = -inf
         const bool st_ok = wait_staging();
         if (exchange(st_ok ? 0u : 2u, false, 0.f) & 2u) { aborted = true; break; }
-        uint8_t* ob = obuf_of(static_cast<int>(k_out & 1u));
-        if (r < HEAD_DIM) {
+        uint8_t* ob = obuf_of(static_cast<int>(k_out % NB));
+        for (int dr = r; dr < HEAD_DIM; dr += 128) {  // rows r (and r + 128 for head_dim 256)
           for (int n = c0; n < c0 + NC && n < nv; ++n) {
             if (it.slot < 0 && p.out_dtype != kOutF32)
-              reinterpret_cast<__nv_bfloat16*>(ob)[n * HEAD_DIM + r] = __float2bfloat16_rn(0.f);  // +0: all-zero bits
+              reinterpret_cast<__nv_bfloat16*>(ob)[n * HEAD_DIM + dr] = __float2bfloat16_rn(0.f);  // +0: all-zero bits
             else
-              reinterpret_cast<float*>(ob)[n * HEAD_DIM + r] = 0.f;
+              reinterpret_cast<float*>(ob)[n * HEAD_DIM + dr] = 0.f;
           }
         }
-        if (r >= c0 && r < c0 + NC && r < nv) lse_of(static_cast<int>(k_out & 1u))[r] = -INFINITY;
-        hand_over(it);
+        if (r >= c0 && r < c0 + NC && r < nv) lse_of(static_cast<int>(k_out % NB))[r] = -INFINITY;
+        if (!hand_over(it)) { aborted = true; break; }
         continue;
       }
       const int L = it.L;
@@ -1018,17 +1218,31 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           const int tail_rows = L - blk * kBlockN;
           const int cap_rows = plan.max_seqlen - blk * kBlockN;
           if (wg == 0 && tail_rows < kBlockN && cap_rows > tail_rows) {
-            // Wait for V(g) to land.  PV(g-2) is done, so V(g - NSV) was
-            // consumed and this parity wait cannot pass a phase early.
-            const uint32_t stage = NSK + g % NSV;
-            local_abort = !ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (g / NSV) & 1u, abort_flag, p.timeout_ns);
-            local_abort = __any_sync(0xffffffffu, local_abort);
-            if (!local_abort && r >= tail_rows && r < cap_rows) {
+            // Wait for V(g)'s tiles to land.  A parity wait is sound once the
+            // previous tile of the same stage (NSV tiles earlier) has landed:
+            // PV(g-2) is done, which covers it when a ring stage pair holds
+            // two blocks; with two tiles per block (head_dim 256) the ring
+            // holds one block and PV(g-1) must be done as well.
+            if constexpr (TPB > 1) {
+              if (!local_abort && g >= 1)
+                local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u,
+                                                      abort_flag, p.timeout_ns);
+            }
 #pragma unroll
-              for (int kc = 0; kc < KCH; ++kc) {
-                uint4* row = reinterpret_cast<uint4*>(ring + stage * Cfg::kSlotBytes + kc * 16384 + r * 128);
+            for (int hf = 0; hf < TPB; ++hf) {
+              const uint32_t u = g * TPB + static_cast<uint32_t>(hf);
+              const uint32_t stage = NSK + u % NSV;
+              if (!local_abort)
+                local_abort = !ptx::mbar_wait_bounded(BAR(RING_FULL + stage), (u / NSV) & 1u, abort_flag,
+                                                      p.timeout_ns);
+              local_abort = __any_sync(0xffffffffu, local_abort);
+              if (!local_abort && r >= tail_rows && r < cap_rows) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                for (int kc = 0; kc < TCH; ++kc) {
+                  uint4* row = reinterpret_cast<uint4*>(ring + stage * Cfg::kSlotBytes + kc * 16384 + r * 128);
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                }
               }
             }
           }
@@ -1055,7 +1269,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       xcombine(lt, false);
 
       ptx::tc_fence_after();
-      constexpr int kHalves = Cfg::kOWidth / NPAD;  // 2 for head_dim 64 (stacked half-blocks)
+      // 2 for head_dim 64 (stacked position halves, added below) and 256
+      // (d-halves: rows r and r + 128 of O)
+      constexpr int kHalves = Cfg::kOWidth / NPAD;
       float o[kHalves * NC];
 #pragma unroll
       for (int h2 = 0; h2 < kHalves; ++h2) {
@@ -1094,20 +1310,25 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         // fp32 for partials and fp32 outputs, else 16-bit outputs of the
         // input type
         const bool out16 = it.slot < 0 && p.out_dtype != kOutF32;
-        uint8_t* obuf = obuf_of(static_cast<int>(k_out & 1u));
+        uint8_t* obuf = obuf_of(static_cast<int>(k_out % NB));
+        constexpr int kRowsOut = HEAD_DIM == 256 ? 2 : 1;  // O rows of this thread: r (+ 128)
 #pragma unroll
         for (int n = 0; n < NC; ++n) {
           const float inv = lt[n] > 0.f ? ptx::rcp_approx(lt[n]) : 0.f;
-          const float val = o[n] * inv;
           const int ng = c0 + n;
           if (ng < nv) {
-            if (out16) {
-              if constexpr (IN_F16)
-                reinterpret_cast<__half*>(obuf)[ng * HEAD_DIM + d_row] = __float2half_rn(val);
-              else
-                reinterpret_cast<__nv_bfloat16*>(obuf)[ng * HEAD_DIM + d_row] = __float2bfloat16_rn(val);
-            } else {
-              reinterpret_cast<float*>(obuf)[ng * HEAD_DIM + d_row] = val;
+#pragma unroll
+            for (int h2 = 0; h2 < kRowsOut; ++h2) {
+              const float val = o[h2 * NC + n] * inv;
+              const int dr = d_row + 128 * h2;
+              if (out16) {
+                if constexpr (IN_F16)
+                  reinterpret_cast<__half*>(obuf)[ng * HEAD_DIM + dr] = __float2half_rn(val);
+                else
+                  reinterpret_cast<__nv_bfloat16*>(obuf)[ng * HEAD_DIM + dr] = __float2bfloat16_rn(val);
+              } else {
+                reinterpret_cast<float*>(obuf)[ng * HEAD_DIM + dr] = val;
+              }
             }
           }
         }
@@ -1116,14 +1337,22 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
           for (int n = 0; n < NC; ++n)
             if (c0 + n == d_row) { lt_n = lt[n]; m_n = m[n]; }
-          lse_of(static_cast<int>(k_out & 1u))[d_row] =
+          lse_of(static_cast<int>(k_out % NB))[d_row] =
               lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
         }
       }
-      hand_over(it);
+      if (!hand_over(it)) { aborted = true; break; }
     }
     if constexpr (!kPvStores) {
       if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_all();  // this CTA's outputs are in global memory
+    }
+    if (cluster_merge && threadIdx.x == sm0) {
+      // The other CTAs read this CTA's staging buffers until they arrive on
+      // PEER_EMPTY: the CTA may not exit before (bounded waits).
+      for (uint32_t i = k_out >= NB ? k_out - NB : 0u; i < k_out; ++i)
+        ptx::mbar_wait_cluster_bounded(BAR(PEER_EMPTY + 2 * wg + static_cast<int>(i % NB)), (i / NB) & 1u,
+                                       abort_flag, p.timeout_ns);
+      ptx::bulk_wait_all();  // this warpgroup's merged outputs are in global memory
     }
     if (aborted || local_abort) detail::set_error(kErrTimeout, abort_flag);
     ptx::griddep_launch_dependents();

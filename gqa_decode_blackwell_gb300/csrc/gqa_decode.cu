@@ -98,7 +98,9 @@ gqa_status_t check_desc(const gqa_desc_t* d) {
   // a 16-bit output has the inputs' type (fp32 goes with either)
   if (d->out_dtype != GQA_DTYPE_FP32 && d->out_dtype != d->in_dtype) return GQA_ERR_UNSUPPORTED;
   if (!(d->scale >= 0.f) || std::isinf(d->scale)) return GQA_ERR_INVALID_ARG;
-  if (d->head_dim != 64 && d->head_dim != 128) return GQA_ERR_UNSUPPORTED;
+  if (d->reduction != GQA_REDUCE_AUTO && d->reduction != GQA_REDUCE_COMBINE && d->reduction != GQA_REDUCE_CLUSTER)
+    return GQA_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return GQA_ERR_UNSUPPORTED;
   const long long g = d->q_heads / d->kv_heads;
   if (static_cast<long long>(d->q_tokens) * g > GQA_MAX_QROWS) return GQA_ERR_UNSUPPORTED;
   if (d->q_heads > 65535 || d->max_seqlen > (1 << 30)) return GQA_ERR_UNSUPPORTED;
@@ -110,7 +112,16 @@ struct HostPlan {
   int num_slots;      // partial slots per row (0: the decode writes final outputs only)
   bool combine;       // a combine launch follows
   bool use_n_pieces;  // combine reads per-pair piece counts (balanced plan)
+  int cluster_k;      // > 1: the k splits of a pair form a cluster and merge in it
+  gqa_status_t status;  // GQA_ERR_UNSUPPORTED: an in-cluster merge was asked for and cannot be done
 };
+
+// Largest power of two <= x, for 1 <= x (capped at kMaxClusterK).
+int pow2_floor_k(long long x) {
+  int k = 1;
+  while (2LL * k <= x && k < kMaxClusterK) k *= 2;
+  return k;
+}
 
 // Automatic split count for the fixed-splits plan, from a load model that
 // assumes every sequence is max_seqlen long: the busiest CTA's blocks plus
@@ -139,9 +150,40 @@ int auto_splits(long long pairs, int nblk, int rows_per_pair, int head_dim, int 
 constexpr int kItemUnits16 = 1;
 constexpr int kItemUnits32 = 3;
 
+// Cluster size of the in-cluster merge ("Building a Faster GQA Decode Kernel
+// for Blackwell SM100", section "Reducing inside a thread block cluster":
+// the KV splits of one batch entry and head group form a cluster; automatic
+// selection takes it for at most four splits, or eight with at most 64 CTAs).
+// Returns 0 when the kernel-reduction plans (combine launch) are to be used,
+// else the number k >= 1 of splits per pair, and -1 for a forced in-cluster
+// merge that cannot be done (a split count that is not a power of two <= 8).
+int cluster_splits(const gqa_desc_t* d, int num_splits, int sm, bool force_partial) {
+  if (force_partial || d->reduction == GQA_REDUCE_COMBINE) return 0;
+  const bool forced = d->reduction == GQA_REDUCE_CLUSTER;
+  const long long pairs = static_cast<long long>(d->batch) * d->kv_heads;
+  const int nblk_cap = num_blocks(d->max_seqlen);
+  if (num_splits == 0) {
+    // the whole-CTAs-per-pair shape of the automatic plan, k a power of two
+    const long long per_pair = pairs > 0 ? sm / pairs : 0;
+    const long long lim = per_pair < nblk_cap ? per_pair : nblk_cap;
+    const int k = lim >= 1 ? pow2_floor_k(lim) : 1;
+    if (forced) return k;
+    // Only where the cluster grid keeps at least half the CTAs of the
+    // automatic balanced plan (k whole CTAs per pair, or one per block):
+    // one long pair, say, is spread over every SM there, not over 8.
+    const long long bal_ctas = per_pair * pairs < pairs * nblk_cap ? per_pair * pairs : pairs * nblk_cap;
+    const bool short_seqs = nblk_cap <= 32 * k;
+    return (k >= 2 && short_seqs && 2 * k * pairs >= bal_ctas && (k <= 4 || pairs * k <= 64)) ? k : 0;
+  }
+  const bool pow2 = (num_splits & (num_splits - 1)) == 0;
+  if (forced) return (pow2 && num_splits <= kMaxClusterK) ? num_splits : -1;
+  return (num_splits >= 2 && pow2 && (num_splits <= 4 || (num_splits == 8 && pairs * 8 <= 64))) ? num_splits : 0;
+}
+
 HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_partial) {
   HostPlan hp;
   std::memset(&hp, 0, sizeof hp);
+  hp.status = GQA_OK;
   PlanParams& pp = hp.pp;
   pp.batch = d->batch;
   pp.kv_heads = d->kv_heads;
@@ -150,6 +192,31 @@ HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_parti
   const long long pairs = static_cast<long long>(d->batch) * d->kv_heads;
   const int rows_per_pair = d->q_tokens * (d->q_heads / d->kv_heads);
   const int item_units = rows_per_pair <= 16 ? kItemUnits16 : kItemUnits32;
+  const int ck = cluster_splits(d, num_splits, sm, force_partial);
+  if (ck < 0) {
+    hp.status = GQA_ERR_UNSUPPORTED;
+    return hp;
+  }
+  if (ck >= 1) {
+    // Fixed splits, k per pair, dealt so that the CTAs of one cluster take
+    // the k pieces of the same pairs: a persistent grid of up to #SMs / k
+    // clusters, cluster q walking pairs q, q + clusters, ...  (CTA q*k + j
+    // holds piece j).  The pieces meet in the cluster's shared memory; no
+    // partials reach global memory and no combine launch follows.
+    pp.mode = PLAN_SPLITS;
+    pp.num_splits = ck;
+    pp.min_blocks = 1;
+    pp.force_partial = ck > 1 ? 1 : 0;
+    long long clusters = sm / ck;
+    if (clusters < 1) clusters = 1;
+    if (clusters > pairs) clusters = pairs > 0 ? pairs : 1;
+    pp.num_ctas = static_cast<int>(clusters * ck);
+    hp.num_slots = 0;
+    hp.combine = false;
+    hp.use_n_pieces = false;
+    hp.cluster_k = ck;
+    return hp;
+  }
   // the balanced plan keeps per-sequence unit prefix sums in int32
   const bool pre_fits = static_cast<long long>(d->batch) * pair_units(nblk_cap, item_units) <= 0x7fffffffLL;
   if (num_splits == 0 && d->batch <= kMaxSmemB && pre_fits) {
@@ -206,7 +273,65 @@ WsLayout ws_layout(const gqa_desc_t* d, const HostPlan& hp) {
   return w;
 }
 
+// Tensor maps of recent (q, k_cache, v_cache) pointer and shape combinations.
+// A map is a pure function of its key (base address, dims, strides, type), so
+// an entry stays valid for any buffer that later occupies the same address
+// with the same shape; nothing needs invalidating.  Saves the three
+// cuTensorMapEncodeTiled calls of an eager decode call that repeats its
+// buffers (a decode loop over one KV cache).
+struct MapKey {
+  const void* q;
+  const void* k;
+  const void* v;
+  int batch, q_tokens, q_heads, kv_heads, head_dim, max_seqlen, in_dtype;
+  bool operator==(const MapKey& o) const {
+    return q == o.q && k == o.k && v == o.v && batch == o.batch && q_tokens == o.q_tokens &&
+           q_heads == o.q_heads && kv_heads == o.kv_heads && head_dim == o.head_dim &&
+           max_seqlen == o.max_seqlen && in_dtype == o.in_dtype;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  bool valid;
+  CUtensorMap tm_q, tm_k, tm_v;
+};
+constexpr int kMapCacheEntries = 64;
+std::mutex g_map_mu;
+MapEntry g_map_cache[kMapCacheEntries];
+unsigned g_map_next = 0;
+
+gqa_status_t encode_maps_uncached(const gqa_desc_t* d, const void* q, const void* k, const void* v,
+                                  DecodeParams* p);
+
 gqa_status_t encode_maps(const gqa_desc_t* d, const void* q, const void* k, const void* v, DecodeParams* p) {
+  const MapKey key{q, k, v, d->batch, d->q_tokens, d->q_heads, d->kv_heads, d->head_dim, d->max_seqlen,
+                   d->in_dtype};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < kMapCacheEntries; ++i) {
+      const MapEntry& e = g_map_cache[i];
+      if (e.valid && e.key == key) {
+        p->tm_q = e.tm_q;
+        p->tm_k = e.tm_k;
+        p->tm_v = e.tm_v;
+        return GQA_OK;
+      }
+    }
+  }
+  const gqa_status_t rc = encode_maps_uncached(d, q, k, v, p);
+  if (rc != GQA_OK) return rc;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  MapEntry& e = g_map_cache[g_map_next++ % kMapCacheEntries];
+  e.key = key;
+  e.tm_q = p->tm_q;
+  e.tm_k = p->tm_k;
+  e.tm_v = p->tm_v;
+  e.valid = true;
+  return GQA_OK;
+}
+
+gqa_status_t encode_maps_uncached(const gqa_desc_t* d, const void* q, const void* k, const void* v,
+                                  DecodeParams* p) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return GQA_ERR_CUDA;
   const cuuint64_t D = static_cast<cuuint64_t>(d->head_dim);
@@ -259,9 +384,18 @@ gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodePar
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
-  cfg.attrs = &attr;
+  cudaLaunchAttribute attrs[2];
+  attrs[0] = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
+  cfg.attrs = attrs;
   cfg.numAttrs = 1;
+  if (p.cluster_k > 1) {
+    std::memset(&attrs[1], 0, sizeof attrs[1]);
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = static_cast<unsigned>(p.cluster_k);
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   if (cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HD, NP, F16>, p) != cudaSuccess) return GQA_ERR_CUDA;
   return GQA_OK;
 }
@@ -269,9 +403,12 @@ gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodePar
 template <bool F16>
 gqa_status_t launch_decode_dt(DeviceState* st, const DecodeParams& p, cudaStream_t s) {
   const int nv = p.nq * p.G;
-  const unsigned b = F16 ? 4u : 0u;
+  const unsigned b = F16 ? 6u : 0u;
   if (p.head_dim == 64) {
     return nv <= 16 ? launch_decode_t<64, 16, F16>(st, b + 0, p, s) : launch_decode_t<64, 32, F16>(st, b + 1, p, s);
+  }
+  if (p.head_dim == 256) {
+    return nv <= 16 ? launch_decode_t<256, 16, F16>(st, b + 4, p, s) : launch_decode_t<256, 32, F16>(st, b + 5, p, s);
   }
   return nv <= 16 ? launch_decode_t<128, 16, F16>(st, b + 2, p, s) : launch_decode_t<128, 32, F16>(st, b + 3, p, s);
 }
@@ -293,8 +430,9 @@ gqa_status_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t s
   cudaLaunchAttribute attr = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  cudaError_t e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, gqa_combine_kernel<64>, c)
-                                 : cudaLaunchKernelEx(&cfg, gqa_combine_kernel<128>, c);
+  cudaError_t e = head_dim == 64    ? cudaLaunchKernelEx(&cfg, gqa_combine_kernel<64>, c)
+                  : head_dim == 256 ? cudaLaunchKernelEx(&cfg, gqa_combine_kernel<256>, c)
+                                    : cudaLaunchKernelEx(&cfg, gqa_combine_kernel<128>, c);
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -321,6 +459,7 @@ gqa_status_t prepare_decode(const gqa_desc_t* d, const void* q, const void* k, c
   const float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
   p->scale_log2 = scale * 1.4426950408889634f;
   p->lse_bulk = (p->G % 4) == 0;  // LSE rows of G floats: 16-byte multiples
+  p->cluster_k = hp.cluster_k > 1 ? hp.cluster_k : 0;
   p->timeout_ns = wait_timeout_ns();
   return GQA_OK;
 }
@@ -350,6 +489,7 @@ size_t gqa_decode_workspace_size(const gqa_desc_t* desc, int num_splits) {
   DeviceState* st = nullptr;
   if (current_device(&dev, &st) != GQA_OK) return 0;
   const HostPlan hp = make_plan(desc, num_splits, st->sm_count, false);
+  if (hp.status != GQA_OK) return 0;
   return ws_layout(desc, hp).total;
 }
 
@@ -373,6 +513,7 @@ gqa_status_t attn_impl(const gqa_desc_t* desc, const void* q, const void* k_cach
   DeviceState* st = nullptr;
   if ((rc = current_device(&dev, &st)) != GQA_OK) return rc;
   const HostPlan hp = make_plan(desc, num_splits, st->sm_count, false);
+  if (hp.status != GQA_OK) return hp.status;
   const WsLayout wl = ws_layout(desc, hp);
   if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total || !aligned(workspace, kWsAlign)))
     return GQA_ERR_WORKSPACE;
@@ -476,7 +617,9 @@ gqa_status_t gqa_decode_attn_static_workspace(const gqa_desc_t* desc, const void
   int dev = 0;
   DeviceState* st = nullptr;
   if ((rc = current_device(&dev, &st)) != GQA_OK) return rc;
-  const size_t need = ws_layout(desc, make_plan(desc, num_splits, st->sm_count, false)).total;
+  const HostPlan hp = make_plan(desc, num_splits, st->sm_count, false);
+  if (hp.status != GQA_OK) return hp.status;
+  const size_t need = ws_layout(desc, hp).total;
   if (need > GQA_STATIC_WORKSPACE_BYTES) return GQA_ERR_WORKSPACE;  // larger than the static array
   void* ws = nullptr;
   if ((rc = static_workspace_ptr(dev, &ws)) != GQA_OK) return rc;
@@ -510,7 +653,7 @@ gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const voi
 gqa_status_t gqa_decode_combine(const float* o_part, const float* lse_part, int num_splits, int64_t rows,
                                 int head_dim, void* out, int out_dtype, float* lse, void* stream) {
   if (num_splits < 1 || num_splits > GQA_MAX_SPLITS || rows < 0) return GQA_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128) return GQA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return GQA_ERR_UNSUPPORTED;
   if (out_dtype != GQA_DTYPE_BF16 && out_dtype != GQA_DTYPE_FP32 && out_dtype != GQA_DTYPE_FP16)
     return GQA_ERR_INVALID_ARG;
   if (rows == 0) return GQA_OK;
@@ -570,8 +713,9 @@ gqa_status_t gqa_decode_plan(const gqa_desc_t* desc, const int32_t* seqlens_host
     sm_count = st->sm_count;
   }
   const HostPlan hp = make_plan(desc, num_splits, sm_count, false);
+  if (hp.status != GQA_OK) return hp.status;
   if (num_ctas) *num_ctas = hp.pp.num_ctas;
-  if (plan_mode) *plan_mode = hp.pp.mode;
+  if (plan_mode) *plan_mode = hp.cluster_k > 1 ? 2 : hp.pp.mode;
   if (num_slots) *num_slots = hp.combine ? hp.num_slots : 0;
   const int B = desc->batch;
   std::vector<int32_t> clamped(static_cast<size_t>(B > 0 ? B : 1)), pre(static_cast<size_t>(B) + 1, 0);

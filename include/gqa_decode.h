@@ -59,6 +59,28 @@ typedef enum {
 
 typedef enum { GQA_DTYPE_BF16 = 0, GQA_DTYPE_FP32 = 1, GQA_DTYPE_FP16 = 2 } gqa_dtype_t;
 
+/* How the split partials of a sequence are merged ("Building a Faster GQA
+ * Decode Kernel for Blackwell SM100", sections "Combining the KV splits" and
+ * "Reducing inside a thread block cluster"):
+ *   GQA_REDUCE_COMBINE  the decode kernel writes fp32 partials to the
+ *                       workspace and a second kernel merges them;
+ *   GQA_REDUCE_CLUSTER  the k splits of one (batch, KV head) pair run as one
+ *                       thread-block cluster and merge their partials in the
+ *                       cluster's distributed shared memory, in a fixed split
+ *                       order, each CTA writing d/k columns of the output: no
+ *                       workspace, no second launch, nothing to zero, results
+ *                       bit-identical from run to run.  Needs k = num_splits
+ *                       a power of two <= 8 (num_splits = 0: the largest
+ *                       power of two <= min(8, #SMs / pairs, blocks));
+ *                       otherwise GQA_ERR_UNSUPPORTED;
+ *   GQA_REDUCE_AUTO     the page's selection: the in-cluster merge for at most
+ *                       four splits, or eight with at most 64 CTAs; with
+ *                       num_splits = 0, when the automatic plan would give
+ *                       every pair k >= 2 whole CTAs of at most 32 blocks
+ *                       each (short sequences) and the k * pairs CTAs are at
+ *                       least half of that plan's, else the combine kernel. */
+typedef enum { GQA_REDUCE_AUTO = 0, GQA_REDUCE_COMBINE = 1, GQA_REDUCE_CLUSTER = 2 } gqa_reduction_t;
+
 /* Problem description.  Q is [batch, q_tokens, q_heads, head_dim]; the K
  * and V caches are [batch, max_seqlen, kv_heads, head_dim]; all three are
  * in_dtype (bf16 or fp16).  Scores, softmax and accumulation are fp32; P
@@ -75,6 +97,7 @@ typedef struct {
   int out_dtype;   /* gqa_dtype_t of `out`: FP32, or in_dtype (a 16-bit
                       output of the other 16-bit type is GQA_ERR_UNSUPPORTED) */
   int in_dtype;    /* gqa_dtype_t of q, k_cache, v_cache: BF16 or FP16 */
+  int reduction;   /* gqa_reduction_t: how split partials are merged (0 = auto) */
 } gqa_desc_t;
 
 /* Limits: q_tokens * (q_heads / kv_heads) <= 32 query rows per KV head, and
@@ -89,7 +112,8 @@ typedef struct {
  * section "Combining the KV splits").  num_splits: 0 = automatic, 1..64 =
  * exactly that many contiguous 128-position-aligned splits per sequence.
  * Returns 0 when no workspace is needed (a single split), and also for an
- * invalid description.  Depends on the current device (its SM count).
+ * invalid description.  Depends on the current device (its SM count).  The
+ * in-cluster merge needs none.
  */
 size_t gqa_decode_workspace_size(const gqa_desc_t* desc, int num_splits);
 
@@ -225,7 +249,9 @@ const char* gqa_status_string(gqa_status_t status);
  * Host-side view of the work decomposition the decode kernel will use, for
  * inspection and testing.  seqlens_host: int32 [B] in host memory; sm_count:
  * SMs to plan for (0 = those of the current device; needs no GPU otherwise).  Fills
- * *num_ctas with the grid size, *plan_mode with 0 (fixed splits per sequence)
+ * *num_ctas with the grid size, *plan_mode with 0 (fixed splits per sequence),
+ * 2 (fixed splits merged inside thread-block clusters of num_splits CTAs,
+ * CTA q*k + j taking piece j of the pairs of cluster q)
  * or 1 (balanced contiguous ranges; each non-empty (b, h) pair counts its
  * 128-position blocks plus X units for the item's fixed cost: X = 0 with a
  * grid of k CTAs per pair when k >= 2 fit on the SMs and S_max spans at most

@@ -46,7 +46,8 @@ def _attn(L, desc, q=ALIGNED, k=ALIGNED, v=ALIGNED, sl=ALIGNED, out=ALIGNED, lse
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(head_dim=96), g.GQA_ERR_UNSUPPORTED),
-    (dict(head_dim=256), g.GQA_ERR_UNSUPPORTED),
+    (dict(head_dim=512), g.GQA_ERR_UNSUPPORTED),
+    (dict(head_dim=192), g.GQA_ERR_UNSUPPORTED),
     (dict(q_heads=6, kv_heads=4), g.GQA_ERR_INVALID_ARG),
     (dict(q_tokens=0), g.GQA_ERR_INVALID_ARG),
     (dict(batch=-1), g.GQA_ERR_INVALID_ARG),

@@ -17,8 +17,9 @@ def _built():
     gbuild.build()
 
 
-def _desc(B, Hkv, s_max, G=4, nq=1, d=128):
-    return g.gqa_desc_t(B, nq, Hkv * G, Hkv, d, s_max, 0.0, 0, 0)
+def _desc(B, Hkv, s_max, G=4, nq=1, d=128, reduction=g.GQA_REDUCE_COMBINE):
+    """The kernel-reduction plans by default (the in-cluster merge has tests of its own below)."""
+    return g.gqa_desc_t(B, nq, Hkv * G, Hkv, d, s_max, 0.0, 0, 0, 0, reduction)
 
 
 def _blocks(L):
@@ -198,3 +199,132 @@ def test_balanced_plan_needs_int32_prefix_sums():
     assert mode == 0
     C, mode, slots, items = g.gqa_decode_plan(_desc(512, 1, 1 << 20), [1] * 512, 0, 152, max_items=0)
     assert mode == 1
+
+
+# ------------------------------------------------------- in-cluster merge
+def _cluster_k_auto(pairs, sm, s_max):
+    """The automatic choice: k = the largest power of two <= min(8, sm // pairs,
+    blocks), taken when k >= 2, the cache spans at most 32 k blocks, the k *
+    pairs CTAs are at least half of the balanced plan's (sm // pairs per pair,
+    at most one per block), and k <= 4 or k * pairs <= 64; else 0 (the
+    combine kernel)."""
+    per_pair = sm // pairs
+    lim = min(per_pair, _blocks(s_max))
+    k = 1
+    while 2 * k <= lim and k < 8:
+        k *= 2
+    bal = min(per_pair * pairs, pairs * _blocks(s_max))
+    if k >= 2 and _blocks(s_max) <= 32 * k and 2 * k * pairs >= bal and (k <= 4 or pairs * k <= 64):
+        return k
+    return 0
+
+
+def check_cluster(lens, Hkv, s_max, sm, k, G=4, nq=1, num_splits=0, reduction=g.GQA_REDUCE_AUTO):
+    """Cluster plan: k fixed splits per pair; CTA q*k + j holds piece j of the
+    pairs q, q + Q, ... of cluster q (Q = grid / k clusters), with the
+    documented partition of each sequence into min(k, blocks) splits."""
+    desc = _desc(len(lens), Hkv, s_max, G=G, nq=nq, reduction=reduction)
+    C, mode, slots, items = g.gqa_decode_plan(desc, lens, num_splits, sm)
+    pairs = len(lens) * Hkv
+    assert mode == 2 and slots == 0
+    Q = max(1, min(pairs, sm // k))
+    assert C == Q * k
+    begin, end = oracle.split_ranges(lens, k, block=128)
+    seen = collections.Counter()
+    for c, b, h, b0, b1, slot, first, npieces in items:
+        q, j = divmod(int(c), k)
+        pair = b * Hkv + h
+        assert pair % Q == q and slot == j
+        L = min(max(lens[b], 0), s_max)
+        if b0 < b1:
+            assert (b0 * 128, min(b1 * 128, L)) == (begin[j, b], end[j, b])
+        else:
+            assert begin[j, b] == end[j, b] == 0 or L == 0
+        seen[(b, h, j)] += 1
+    assert set(seen) == {(b, h, j) for b in range(len(lens)) for h in range(Hkv) for j in range(k)}
+    assert set(seen.values()) == {1}
+
+
+@pytest.mark.parametrize("B,Hkv,L,G,nq,k", [
+    (8, 8, 4096, 4, 1, 2),      # Llama-8B-shaped: 64 pairs, clusters of two
+    (32, 2, 2048, 8, 4, 2),     # speculative
+    (1, 1, 512, 8, 1, 4),       # tiny: four blocks, a cluster of four
+    (8, 1, 1024, 4, 1, 8),      # 8 pairs x 8 <= 64 CTAs, 8 blocks each
+    (4, 8, 8192, 8, 1, 4),      # 32 pairs, 64 blocks <= 32 x 4
+])
+def test_auto_selects_cluster_merge_for_short_sequences(B, Hkv, L, G, nq, k):
+    assert _cluster_k_auto(B * Hkv, 152, L) == k
+    check_cluster([L] * B, Hkv, L, 152, k, G, nq)
+
+
+@pytest.mark.parametrize("B,Hkv,L,G,nq,mode", [
+    (16, 8, 8192, 8, 1, 1),     # 70B-shaped: one SM per pair, balanced plan + combine
+    (4, 8, 131072, 8, 1, 1),    # ragged long context: 1024 blocks > 32 x 4
+    (1, 1, 65536, 4, 1, 1),     # one long sequence
+    (1, 1, 32768, 4, 1, 1),     # one pair: 8 CTAs would be far fewer than the balanced plan's 152
+    (1, 2, 4096, 4, 1, 1),      # 2 pairs: 16 CTAs against 64
+])
+def test_auto_keeps_combine_for_long_sequences_or_many_pairs(B, Hkv, L, G, nq, mode):
+    assert _cluster_k_auto(B * Hkv, 152, L) == 0
+    C, m, slots, items = g.gqa_decode_plan(_desc(B, Hkv, L, G=G, nq=nq, reduction=g.GQA_REDUCE_AUTO), [L] * B, 0,
+                                          152)
+    assert m == mode and slots > 0
+
+
+@pytest.mark.parametrize("S,pairs,expect", [
+    (2, 64, 2), (4, 64, 4), (4, 400, 4), (8, 8, 8), (8, 9, 0), (8, 128, 0), (3, 4, 0), (16, 2, 0), (1, 4, 0),
+])
+def test_explicit_split_counts_follow_the_pages_selection(S, pairs, expect):
+    """At most four splits, or eight with at most 64 CTAs, merge in the
+    cluster (power-of-two counts); other counts use the combine kernel."""
+    lens = [2000] * pairs
+    C, mode, slots, items = g.gqa_decode_plan(_desc(pairs, 1, 2000, reduction=g.GQA_REDUCE_AUTO), lens, S, 152)
+    if expect:
+        assert mode == 2 and slots == 0
+        check_cluster(lens, 1, 2000, 152, expect, num_splits=S)
+    else:
+        assert mode == 0
+
+
+@pytest.mark.parametrize("S", [2, 4, 8])
+def test_forced_cluster_merge_with_ragged_lengths(S):
+    rng = np.random.default_rng(S)
+    lens = rng.integers(0, 3000, size=23).tolist()
+    lens[:3] = [0, 1, 129]          # empty, one block, fewer blocks than splits
+    check_cluster(lens, 3, 3000, 152, S, num_splits=S, reduction=g.GQA_REDUCE_CLUSTER)
+
+
+def test_forced_cluster_merge_many_pairs_is_persistent():
+    """128 pairs x 8 pieces on 152 SMs: 19 clusters of eight, each walking
+    its pairs one after another."""
+    check_cluster([8192] * 16, 8, 8192, 152, 8, G=8, num_splits=8, reduction=g.GQA_REDUCE_CLUSTER)
+
+
+def test_forced_cluster_merge_automatic_split_count():
+    # ragged-like: 32 pairs on 152 SMs -> 4 CTAs per pair
+    check_cluster([131072, 1024, 70000, 5], 8, 131072, 152, 4, reduction=g.GQA_REDUCE_CLUSTER)
+    # more pairs than SMs: one CTA per pair, nothing to merge
+    C, mode, slots, items = g.gqa_decode_plan(_desc(200, 1, 300, reduction=g.GQA_REDUCE_CLUSTER), [300] * 200, 0, 152)
+    assert mode == 0 and slots == 0 and C == 152 and all(int(r[5]) == -1 for r in items)
+
+
+@pytest.mark.parametrize("S", [3, 5, 16, 64])
+def test_forced_cluster_merge_rejects_other_split_counts(S):
+    L = g.lib()
+    import ctypes
+    desc = _desc(2, 2, 1000, reduction=g.GQA_REDUCE_CLUSTER)
+    nc, mode, slots, n = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    sl = np.array([1000, 1000], dtype=np.int32)
+    rc = L.gqa_decode_plan(ctypes.byref(desc), sl.ctypes.data, S, 152, ctypes.byref(nc), ctypes.byref(mode),
+                           ctypes.byref(slots), None, 0, ctypes.byref(n))
+    assert rc == g.GQA_ERR_UNSUPPORTED
+
+
+def test_unknown_reduction_mode_is_invalid():
+    import ctypes
+    desc = _desc(2, 2, 1000, reduction=7)
+    nc, mode, slots, n = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    sl = np.array([1000, 1000], dtype=np.int32)
+    rc = g.lib().gqa_decode_plan(ctypes.byref(desc), sl.ctypes.data, 0, 152, ctypes.byref(nc), ctypes.byref(mode),
+                                 ctypes.byref(slots), None, 0, ctypes.byref(n))
+    assert rc == g.GQA_ERR_INVALID_ARG

@@ -34,18 +34,18 @@ def _setup():
     g.gqa_decode_get_error(clear=True)
 
 
-def _static_call(inp, out, lse, splits, causal):
+def _static_call(inp, out, lse, splits, causal, reduction="combine"):
     """The new entry point, straight through the C ABI."""
-    desc = g.make_desc(inp.q, inp.k_cache, causal=causal, out_dtype=out.dtype)
+    desc = g.make_desc(inp.q, inp.k_cache, causal=causal, out_dtype=out.dtype, reduction=reduction)
     return g.lib().gqa_decode_attn_static_workspace(
         ctypes.byref(desc), inp.q.data_ptr(), inp.k_cache.data_ptr(), inp.v_cache.data_ptr(),
         inp.seqlens.data_ptr(), out.data_ptr(), lse.data_ptr(), splits,
         torch.cuda.current_stream().cuda_stream)
 
 
-def _with_caller_workspace(inp, splits, causal, out_dtype):
+def _with_caller_workspace(inp, splits, causal, out_dtype, reduction="combine"):
     out, lse = g.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, num_splits=splits, causal=causal,
-                        out_dtype=out_dtype)
+                        out_dtype=out_dtype, reduction=reduction)
     return out, lse
 
 
@@ -62,7 +62,10 @@ def _ragged_cut_down():
 def test_static_workspace_matches_caller_workspace_on_consecutive_calls():
     """Consecutive calls share the static array.  Both paths run the same
     plan and the same kernels, so their outputs must be bit-identical; the
-    stated tolerance (2e-2 / 1e-3) would hide a stale slot that leaks in."""
+    stated tolerance (2e-2 / 1e-3) would hide a stale slot that leaks in.
+    The split partials go through the array with the combine kernel as the
+    merge (the in-cluster merge needs no workspace at all: its case checks
+    that the entry point still gives the caller-workspace result)."""
     cases = [("llama8b", 0), ("spec", 0), ("llama70b", 8), ("ragged-cut", 8), ("ragged-cut", 0), ("llama8b", 0)]
     for name, splits in cases:
         if name == "ragged-cut":
@@ -105,3 +108,18 @@ def test_static_workspace_refuses_problems_larger_than_it():
     torch.cuda.synchronize()
     ref_out, ref_lse = _with_caller_workspace(inp, 8, False, torch.bfloat16)
     assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+
+
+def test_static_workspace_with_in_cluster_merge():
+    """Problems the automatic selection merges inside thread-block clusters
+    need no workspace; the entry point then simply runs them."""
+    cfg = workloads.CONFIGS["llama8b"]
+    inp = workloads.make_inputs(cfg).to(DEV)
+    assert g.gqa_decode_workspace_size(inp.q, inp.k_cache, 0, reduction="auto") == 0
+    ref_out, ref_lse = _with_caller_workspace(inp, 0, False, torch.bfloat16, reduction="auto")
+    for _ in range(2):
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        assert _static_call(inp, out, lse, 0, False, reduction="auto") == g.GQA_OK
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
