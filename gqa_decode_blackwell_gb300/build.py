@@ -25,7 +25,7 @@ def _nvcc() -> str:
 
 
 def sources():
-    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cuh"))] + [HEADER]
+    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cuh", ".h"))] + [HEADER]
 
 
 def up_to_date(out: str = LIB) -> bool:
@@ -35,16 +35,39 @@ def up_to_date(out: str = LIB) -> bool:
     return all(os.path.getmtime(s) <= t for s in sources())
 
 
+# Translation units: the host side (C ABI, planning, combine kernel) and one
+# unit per head_dim and merge mode holding that combination's decode kernels,
+# compiled in parallel and linked into one shared library.
+INSTANCES = [(hd, cl) for hd in (64, 128, 256) for cl in (0, 1)]
+
+
+def _units(build_dir: str):
+    units = [(os.path.join(CSRC, "gqa_decode.cu"), [], os.path.join(build_dir, "gqa_decode.o"))]
+    for hd, cl in INSTANCES:
+        units.append((os.path.join(CSRC, "decode_instances.cu"), [f"-DGQA_INST_HD={hd}", f"-DGQA_INST_CLUSTER={cl}"],
+                      os.path.join(build_dir, f"decode_{hd}_{cl}.o")))
+    return units
+
+
 def build(force: bool = False, out: str = LIB, extra_flags=(), verbose: bool = False) -> str:
-    """Compile csrc/gqa_decode.cu for sm_103a into ``out`` (skipped if current)."""
+    """Compile the csrc translation units for sm_103a (in parallel) and link
+    them into ``out`` (skipped if current)."""
     if not force and up_to_date(out):
         return out
-    cmd = [_nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-I", os.path.join(ROOT, "include"), *extra_flags,
-           "-o", out + ".tmp", os.path.join(CSRC, "gqa_decode.cu")]
+    build_dir = os.path.join(os.path.dirname(os.path.abspath(out)), "_build",
+                             os.path.splitext(os.path.basename(out))[0])
+    os.makedirs(build_dir, exist_ok=True)
+    base = [_nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+            "-I", os.path.join(ROOT, "include"), *extra_flags]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+        base.insert(1, "-Xptxas=-v")
+    procs = []
+    for src, defs, obj in _units(build_dir):
+        procs.append((obj, subprocess.Popen([*base, *defs, "-c", src, "-o", obj])))
+    failed = [obj for obj, p in procs if p.wait() != 0]
+    if failed:
+        raise subprocess.CalledProcessError(1, f"nvcc ({', '.join(os.path.basename(f) for f in failed)})")
+    subprocess.run([_nvcc(), ARCH, "-shared", *[obj for obj, _ in procs], "-o", out + ".tmp"], check=True)
     os.replace(out + ".tmp", out)
     return out
 

@@ -61,13 +61,9 @@ namespace gqa {
 
 enum : unsigned { kErrTimeout = 1u, kErrBadSeqlen = 2u };
 
-// Device error word of this library: bits of kErrTimeout / kErrBadSeqlen,
-// read and cleared by the host through gqa_decode_get_error().
-__device__ unsigned int g_gqa_error_bits = 0;
-
 // Optional per-CTA event trace (compile with -DGQA_TRACE): clock64 stamps of
-// each role's per-block steps, written to a buffer the host attaches with
-// gqa_trace_attach().  Compiled out otherwise.
+// each role's per-block steps, written to the buffer the host attaches with
+// gqa_trace_attach() (DecodeParams::trace_buf).  Compiled out otherwise.
 enum TraceEvent : int {
   TR_START = 0, TR_SETUP = 1,
   TR_PROD_WAIT = 2, TR_PROD_K = 3, TR_PROD_V = 4, TR_PROD_PLAN = 5, TR_PROD_Q = 6,
@@ -77,7 +73,6 @@ enum TraceEvent : int {
 };
 constexpr int kTraceBlocks = 64;
 #ifdef GQA_TRACE
-__device__ unsigned long long* g_gqa_trace_buf = nullptr;  // [grid][TR_EVENTS][kTraceBlocks]
 __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uint32_t idx) {
   if (buf == nullptr) return;
   const uint32_t i = idx < static_cast<uint32_t>(kTraceBlocks) ? idx : kTraceBlocks - 1;
@@ -85,7 +80,7 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 }
 // The buffer address is read once per thread (GQA_TRACE_SETUP) so that an
 // event costs a clock read and a store, not a dependent global load.
-#define GQA_TRACE_SETUP() unsigned long long* const gqa_trace_buf_ = ::gqa::g_gqa_trace_buf
+#define GQA_TRACE_SETUP() unsigned long long* const gqa_trace_buf_ = p.trace_buf
 #define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event(gqa_trace_buf_, (ev), (idx))
 #define GQA_TRACE_VALUE(ev, idx, v) \
   do { if (gqa_trace_buf_ != nullptr) gqa_trace_buf_[(static_cast<size_t>(blockIdx.x) * ::gqa::TR_EVENTS + (ev)) * ::gqa::kTraceBlocks + (idx)] = (v); } while (0)
@@ -128,6 +123,8 @@ struct DecodeParams {
   int cluster_k;      // > 1: the CTAs of a k-cluster hold the k pieces of a pair and merge them in
                       // distributed shared memory (fixed splits, k = plan.num_splits)
   unsigned long long timeout_ns;
+  unsigned int* err_word;            // the library's device error word (kErrTimeout | kErrBadSeqlen)
+  unsigned long long* trace_buf;     // -DGQA_TRACE builds: [grid][TR_EVENTS][kTraceBlocks] stamps, or null
 };
 
 template <int HEAD_DIM, int NPAD>
@@ -243,8 +240,8 @@ __device__ __forceinline__ int transpose_col(int lane) {
   return col;
 }
 
-__device__ __forceinline__ void set_error(unsigned bits, volatile int* abort_flag) {
-  atomicOr(&g_gqa_error_bits, bits);
+__device__ __forceinline__ void set_error(unsigned int* word, unsigned bits, volatile int* abort_flag) {
+  atomicOr(word, bits);
   if (abort_flag != nullptr) *abort_flag = 1;
 }
 
@@ -271,10 +268,21 @@ struct ItemSource {
     }
     return iter.next(it);
   }
+  // Whether next() would return another item (the walk is not advanced).
+  __device__ __forceinline__ bool has_next() const {
+    if (count >= 0) return k < count;
+    WorkIter copy = iter;
+    WorkItem w;
+    return copy.next(w);
+  }
 };
 
-// IN_F16: q, k, v (and P) are fp16; otherwise bf16.
-template <int HEAD_DIM, int NPAD, bool IN_F16>
+// IN_F16: q, k, v (and P) are fp16; otherwise bf16.  CLUSTER: the launch
+// is a grid of clusters of p.cluster_k CTAs that merge their split partials
+// in distributed shared memory.  A compile-time choice: the merge's code,
+// present but unused, measurably slows the other plans' softmax loop (1.3 us
+// per call on the 32-column speculative shape).
+template <int HEAD_DIM, int NPAD, bool IN_F16, bool CLUSTER>
 __global__ void __launch_bounds__(DecodeCfg<HEAD_DIM, NPAD>::kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HEAD_DIM, NPAD>;
@@ -313,7 +321,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   auto np_of = [&](int ob) -> int32_t* { return reinterpret_cast<int32_t*>(lse_of(ob) + 32); };
   float* xo_buf = reinterpret_cast<float*>(obuf_of(0) + NB * Cfg::kOutBytes);  // kXoBytes
   uint8_t* fin_buf = obuf_of(0) + NB * Cfg::kOutBytes + Cfg::kXoBytes;         // kFinBytes
-  const bool cluster_merge = p.cluster_k > 1;
+  constexpr bool cluster_merge = CLUSTER;
 
   // barrier indices
   const uint32_t bar_base = ptx::smem_u32(bar);
@@ -361,8 +369,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     if (cluster_merge) {
       for (int i = 0; i < 2 * NWG; ++i) {
-        ptx::mbar_init(BAR(PEER_FULL + i), static_cast<uint32_t>(p.cluster_k));  // one arrival per CTA
-        ptx::mbar_init(BAR(PEER_EMPTY + i), static_cast<uint32_t>(p.cluster_k));
+        // one arrival per warp of the warpgroup in every CTA of the cluster
+        ptx::mbar_init(BAR(PEER_FULL + i), 4u * static_cast<uint32_t>(p.cluster_k));
+        ptx::mbar_init(BAR(PEER_EMPTY + i), 4u * static_cast<uint32_t>(p.cluster_k));
       }
     }
     *abort_flag = 0;
@@ -379,9 +388,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   __syncwarp();
   __syncthreads();  // barriers initialised
   // The other CTAs of the cluster arrive on this CTA's barriers: all of them
-  // must be initialised first.  A hardware barrier over straight-line code
-  // (the cluster's CTAs are scheduled together).
-  if (cluster_merge) ptx::cluster_sync_all();
+  // must be initialised first.  Every thread arrives on the cluster's
+  // hardware barrier here, after straight-line code (the cluster's CTAs are
+  // scheduled together); a thread waits on it only before its first remote
+  // arrival, or at teardown, by when the others have long arrived.
+  if (cluster_merge) ptx::cluster_arrive();
+  bool cluster_waited = !cluster_merge;
 
   // This CTA's work items, 32 candidates at a time (one per lane), written to
   // the shared list by the 32 lanes of one warp.  Owned items form a
@@ -444,7 +456,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       for (int i = lane; i < B; i += 32) {
         const int raw = p.seqlens[i];
         const int L = clamp_len(raw, plan.max_seqlen);
-        if (raw != L) detail::set_error(kErrBadSeqlen, nullptr);
+        if (raw != L) detail::set_error(p.err_word, kErrBadSeqlen, nullptr);
         s_len[i] = L;
       }
       __syncwarp();
@@ -545,14 +557,14 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (ptx::mbar_wait_bounded(BAR(PRE_READY), 0, abort_flag, p.timeout_ns)) {
         build_list(lane);
       } else {
-        detail::set_error(kErrTimeout, abort_flag);
+        detail::set_error(p.err_word, kErrTimeout, abort_flag);
         if (lane == 0) list_hdr[0] = 0;
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(BAR(PLAN_READY));
     }
     if (!ptx::mbar_wait_bounded(BAR(PLAN_READY), 0, abort_flag, p.timeout_ns))
-      detail::set_error(kErrTimeout, abort_flag);
+      detail::set_error(p.err_word, kErrTimeout, abort_flag);
     ptx::tc_fence_before();
     ptx::named_barrier_sync(2, kThreads - 32);
     ptx::tc_fence_after();
@@ -673,7 +685,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       }
       for (int hf = 0; hf < TPB && ok && have_prev; ++hf) ok = load_tile(true, pb, ph, pblk, hf);
       if (!ok) {
-        detail::set_error(kErrTimeout, abort_flag);
+        detail::set_error(p.err_word, kErrTimeout, abort_flag);
         // let the copies already issued land before the CTA exits
         for (uint32_t u = tk > NSK ? tk - NSK : 0u; u < tk; ++u)
           ptx::mbar_wait_bounded(BAR(RING_FULL + u % NSK), (u / NSK) & 1u, nullptr, p.timeout_ns);
@@ -825,7 +837,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         GQA_TRACE_EVENT(TR_SM_E1, 0);
         ptx::griddep_launch_dependents();
       }
-      if (!ok) detail::set_error(kErrTimeout, abort_flag);
+      if (!ok) detail::set_error(p.err_word, kErrTimeout, abort_flag);
       // every MMA this thread issued has completed before TMEM is released
       const uint32_t drain = BAR(DRAIN + (is_qk ? 0 : 1));
       ptx::mma_commit(drain);
@@ -891,7 +903,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     uint32_t k_out = 0;  // items staged
     auto wait_staging = [&]() -> bool {
       if (threadIdx.x != sm0) return true;
-      if (cluster_merge) {
+      if constexpr (cluster_merge) {
         // every CTA of the cluster has read this buffer's rows of the item two before
         if (k_out < NB) return true;
         return ptx::mbar_wait_cluster_bounded(BAR(PEER_EMPTY + 2 * wg + static_cast<int>(k_out % NB)),
@@ -915,22 +927,28 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     // [j d/k, (j+1) d/k) of them -- M = max_s lse_s, w_s = exp(lse_s - M),
     // O = sum_s w_s O_s / sum_s w_s in split order s = 0..k-1, empty pieces
     // (lse = -inf) skipped -- and writes them out; CTA 0 writes the LSEs.
-    // Returns false on a timeout (uniform over the warpgroup).
-    auto cluster_merge_item = [&](const WorkItem& wi) -> bool {
+    // Each warp signals its own staged rows and its own finished reads (the
+    // barriers count 4k arrivals), so no warpgroup barrier sits on the path.
+    // A wait that runs out sets the error word; the merge then carries on
+    // (its outputs are invalid) so that every warp still reaches the
+    // warpgroup's barriers.
+    auto cluster_merge_item = [&](const WorkItem& wi, bool last_item) {
       const uint32_t kc = static_cast<uint32_t>(p.cluster_k);
       const uint32_t crank = ptx::cluster_ctarank();
       const int ob = static_cast<int>(k_out % NB);
       const uint32_t full_bar = BAR(PEER_FULL + 2 * wg + ob);
       const uint32_t empty_bar = BAR(PEER_EMPTY + 2 * wg + ob);
-      ptx::named_barrier_sync(xbar, 128);  // this warpgroup's rows are staged
-      if (threadIdx.x == sm0) {
-        ptx::fence_acq_rel_cluster();
-        for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(full_bar, s2));
-        ptx::bulk_wait_read_all();  // the previous item's output copies have read fin
+      if (!cluster_waited) {  // every CTA's barriers are initialised
+        ptx::cluster_wait();
+        cluster_waited = true;
       }
-      bool ok = ptx::mbar_wait_cluster_bounded(full_bar, (k_out / NB) & 1u, abort_flag, p.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (exchange(ok ? 0u : 2u, false, 0.f) & 2u) return false;
+      __syncwarp();  // this warp's rows are staged
+      if (lane == 0)
+        for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(full_bar, s2));
+      if (!ptx::mbar_wait_cluster_bounded(full_bar, (k_out / NB) & 1u, abort_flag, p.timeout_ns))
+        detail::set_error(p.err_word, kErrTimeout, abort_flag);
+      if (!last_item && threadIdx.x == sm0) ptx::bulk_wait_read_all();  // earlier copies have read fin
+      if (!last_item) ptx::named_barrier_sync(xbar, 128);                 // ... before fin is rewritten
 
       constexpr float kLog2e = 1.4426950408889634f;
       const int dk = HEAD_DIM / static_cast<int>(kc);  // output columns of this CTA
@@ -945,96 +963,116 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         const int col = static_cast<int>(crank) * dk + cg * 4;
         const uint32_t o_loc = ptx::smem_u32(obuf_of(ob)) + static_cast<uint32_t>((n * HEAD_DIM + col) * 4);
         const uint32_t l_loc = ptx::smem_u32(lse_of(ob) + n);
-        // The LSEs of all pieces first (their maximum), then the weighted
-        // rows two pieces at a time: few registers live at once.
+        // every piece's LSE in one round trip, then the rows two at a time
+        float ls[kMaxClusterK];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterK; ++s2)
+          ls[s2] = s2 < static_cast<int>(kc) ? ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, static_cast<uint32_t>(s2)))
+                                             : -INFINITY;
         float M = -INFINITY;
-#pragma unroll 1
-        for (uint32_t s2 = 0; s2 < kc; ++s2)
-          M = fmaxf(M, ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, s2)));
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterK; ++s2) M = fmaxf(M, ls[s2]);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float lse_out = -INFINITY;
         if (M != -INFINITY) {
           float W = 0.f;
-#pragma unroll 1
-          for (uint32_t s2 = 0; s2 < kc; s2 += 2) {
-            // kc is a power of two >= 2: pieces s2 and s2 + 1
-            const float la = ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, s2));
-            const float lb = ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, s2 + 1));
-            const float4 oa = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, s2));
-            const float4 o2 = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, s2 + 1));
-            const float wa = la == -INFINITY ? 0.f : ptx::ex2_approx((la - M) * kLog2e);
-            const float wb = lb == -INFINITY ? 0.f : ptx::ex2_approx((lb - M) * kLog2e);
-            W += wa;
-            if (wa != 0.f) {
-              acc.x += wa * oa.x; acc.y += wa * oa.y; acc.z += wa * oa.z; acc.w += wa * oa.w;
-            }
-            W += wb;
-            if (wb != 0.f) {
-              acc.x += wb * o2.x; acc.y += wb * o2.y; acc.z += wb * o2.z; acc.w += wb * o2.w;
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxClusterK; s2 += 2) {
+            if (s2 < static_cast<int>(kc)) {  // kc is a power of two >= 2: pieces s2 and s2 + 1
+              const float4 oa = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, static_cast<uint32_t>(s2)));
+              const float4 o2 = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, static_cast<uint32_t>(s2 + 1)));
+              const float wa = ls[s2] == -INFINITY ? 0.f : ptx::ex2_approx((ls[s2] - M) * kLog2e);
+              const float wb = ls[s2 + 1] == -INFINITY ? 0.f : ptx::ex2_approx((ls[s2 + 1] - M) * kLog2e);
+              W += wa;
+              if (wa != 0.f) {
+                acc.x += wa * oa.x; acc.y += wa * oa.y; acc.z += wa * oa.z; acc.w += wa * oa.w;
+              }
+              W += wb;
+              if (wb != 0.f) {
+                acc.x += wb * o2.x; acc.y += wb * o2.y; acc.z += wb * o2.z; acc.w += wb * o2.w;
+              }
             }
           }
           const float inv = 1.0f / W;
           acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
           lse_out = M + 0.69314718055994531f * __log2f(W);
         }
-        const int e = (n - c0) * dk + cg * 4;  // element of this warpgroup's merged rows
+        const int t = n / p.G;
+        const long long grow =
+            (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G + (n - t * p.G);
+        uint2 packed = make_uint2(0u, 0u);
         if (out16) {
-          uint32_t w2[2];
           if constexpr (IN_F16) {
             __half2 a = __floats2half2_rn(acc.x, acc.y), b2 = __floats2half2_rn(acc.z, acc.w);
-            w2[0] = *reinterpret_cast<uint32_t*>(&a);
-            w2[1] = *reinterpret_cast<uint32_t*>(&b2);
+            packed = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b2));
           } else {
             __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b2 = __floats2bfloat162_rn(acc.z, acc.w);
-            w2[0] = *reinterpret_cast<uint32_t*>(&a);
-            w2[1] = *reinterpret_cast<uint32_t*>(&b2);
+            packed = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b2));
           }
-          *reinterpret_cast<uint2*>(fin_w + e * 2) = make_uint2(w2[0], w2[1]);
+        }
+        if (last_item) {
+          // Nothing of this CTA is still streaming in: plain stores, straight
+          // from registers (16- or 8-byte aligned: col is a multiple of 4).
+          if (out16)
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + grow * HEAD_DIM + col) = packed;
+          else
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + grow * HEAD_DIM + col) = acc;
+          if (crank == 0 && cg == 0 && p.lse != nullptr) p.lse[grow] = lse_out;
         } else {
-          *reinterpret_cast<float4*>(fin_w + e * 4) = acc;
+          const int e = (n - c0) * dk + cg * 4;  // element of this warpgroup's merged rows
+          if (out16) *reinterpret_cast<uint2*>(fin_w + e * 2) = packed;
+          else *reinterpret_cast<float4*>(fin_w + e * 4) = acc;
+          if (crank == 0 && cg == 0) fin_lse[n] = lse_out;
         }
-        if (crank == 0 && cg == 0) fin_lse[n] = lse_out;
       }
-      ptx::fence_proxy_async_smem();       // the merged rows are read by bulk copies
-      ptx::named_barrier_sync(xbar, 128);  // every peer load of this item is done
-      if (threadIdx.x == sm0) {
+      __syncwarp();  // this warp's reads of the other CTAs' rows are done
+      if (lane == 0)
         for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(empty_bar, s2));
-        const uint32_t esz = out16 ? 2u : 4u;
-        const uint32_t slice = static_cast<uint32_t>(dk) * esz;
-        const int n_end = c0 + NC < nv ? c0 + NC : nv;
-        for (int n2 = c0; n2 < n_end; ++n2) {
-          const int t = n2 / p.G, g2 = n2 - t * p.G;
-          const long long grow =
-              (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G + g2;
-          ptx::bulk_store(static_cast<uint8_t*>(p.out) + (grow * HEAD_DIM + static_cast<long long>(crank) * dk) * esz,
-                          ptx::smem_u32(fin_w + (n2 - c0) * slice), slice);
-        }
-        if (crank == 0 && p.lse != nullptr) {
-          // runs of rows of one query token are contiguous in lse
-          for (int n2 = c0; n2 < n_end;) {
-            const int t = n2 / p.G;
-            const int run_end = (t + 1) * p.G < n_end ? (t + 1) * p.G : n_end;
-            const long long grow = (static_cast<long long>(wi.b) * p.nq + t) * p.Hq +
-                                   static_cast<long long>(wi.h) * p.G + (n2 - t * p.G);
-            if (p.lse_bulk) {
-              ptx::bulk_store(p.lse + grow, ptx::smem_u32(fin_lse + n2), static_cast<uint32_t>(run_end - n2) * 4u);
-            } else {
-              for (int i = n2; i < run_end; ++i) p.lse[grow + (i - n2)] = fin_lse[i];
-            }
-            n2 = run_end;
+      if (!last_item) {
+        // Later items still stream K/V tiles into this SM, and plain stores
+        // would queue behind them: the merged rows leave by bulk copies.
+        ptx::fence_proxy_async_smem();       // the merged rows are read by bulk copies
+        ptx::named_barrier_sync(xbar, 128);  // every warp's rows are in fin
+        if (threadIdx.x == sm0) {
+          const uint32_t esz = out16 ? 2u : 4u;
+          const uint32_t slice = static_cast<uint32_t>(dk) * esz;
+          const int n_end = c0 + NC < nv ? c0 + NC : nv;
+          for (int n2 = c0; n2 < n_end; ++n2) {
+            const int t = n2 / p.G, g2 = n2 - t * p.G;
+            const long long grow =
+                (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G + g2;
+            ptx::bulk_store(static_cast<uint8_t*>(p.out) + (grow * HEAD_DIM + static_cast<long long>(crank) * dk) * esz,
+                            ptx::smem_u32(fin_w + (n2 - c0) * slice), slice);
           }
+          if (crank == 0 && p.lse != nullptr) {
+            // runs of rows of one query token are contiguous in lse
+            for (int n2 = c0; n2 < n_end;) {
+              const int t = n2 / p.G;
+              const int run_end = (t + 1) * p.G < n_end ? (t + 1) * p.G : n_end;
+              const long long grow = (static_cast<long long>(wi.b) * p.nq + t) * p.Hq +
+                                     static_cast<long long>(wi.h) * p.G + (n2 - t * p.G);
+              if (p.lse_bulk) {
+                ptx::bulk_store(p.lse + grow, ptx::smem_u32(fin_lse + n2), static_cast<uint32_t>(run_end - n2) * 4u);
+              } else {
+                for (int i = n2; i < run_end; ++i) p.lse[grow + (i - n2)] = fin_lse[i];
+              }
+              n2 = run_end;
+            }
+          }
+          ptx::bulk_commit();
         }
-        ptx::bulk_commit();
       }
       ++k_out;
-      return true;
     };
 
     // Makes the staged rows visible to the async proxy and writes them out
     // (or hands them to the value-MMA thread, or merges them in the cluster).
     // Returns false on a timeout.
-    auto hand_over = [&](const WorkItem& wi) -> bool {
-      if (cluster_merge) return cluster_merge_item(wi);
+    auto hand_over = [&](const WorkItem& wi, bool last_item) -> bool {
+      if constexpr (cluster_merge) {
+        cluster_merge_item(wi, last_item);
+        return true;
+      }
       ptx::fence_proxy_async_smem();
       ptx::named_barrier_sync(xbar, 128);
       if (threadIdx.x == sm0) {
@@ -1065,7 +1103,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           }
         }
         if (r >= c0 && r < c0 + NC && r < nv) lse_of(static_cast<int>(k_out % NB))[r] = -INFINITY;
-        if (!hand_over(it)) { aborted = true; break; }
+        if (!hand_over(it, !iter.has_next())) { aborted = true; break; }
         continue;
       }
       const int L = it.L;
@@ -1341,7 +1379,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
               lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
         }
       }
-      if (!hand_over(it)) { aborted = true; break; }
+      if (!hand_over(it, !iter.has_next())) { aborted = true; break; }
     }
     if constexpr (!kPvStores) {
       if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_all();  // this CTA's outputs are in global memory
@@ -1354,11 +1392,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
                                        abort_flag, p.timeout_ns);
       ptx::bulk_wait_all();  // this warpgroup's merged outputs are in global memory
     }
-    if (aborted || local_abort) detail::set_error(kErrTimeout, abort_flag);
+    if (aborted || local_abort) detail::set_error(p.err_word, kErrTimeout, abort_flag);
     ptx::griddep_launch_dependents();
   }
 
   // ---------------------------------------------------------------- teardown
+  if (!cluster_waited) ptx::cluster_wait();
 #ifdef GQA_TRACE
   if (lane == 0) atomicAdd(&trace_warps_done, 1u);
 #endif

@@ -13,9 +13,16 @@
 #include "../../include/gqa_decode.h"
 #include "combine_kernel.cuh"
 #include "decode_kernel.cuh"
+#include "decode_launch.h"
 #include "plan.cuh"
 
 namespace gqa {
+
+// Device error word of this library: bits of kErrTimeout / kErrBadSeqlen,
+// set by the kernels (through the address each decode launch is given) and
+// read and cleared by gqa_decode_get_error().
+__device__ unsigned int g_gqa_error_bits = 0;
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -23,7 +30,8 @@ constexpr size_t kWsAlign = 256;
 
 struct DeviceState {
   int sm_count = 0;
-  unsigned attr_done = 0;  // one bit per kernel instantiation
+  unsigned attr_done = 0;          // one bit per kernel instantiation
+  unsigned int* err_word = nullptr;  // device address of g_gqa_error_bits
 };
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -76,6 +84,24 @@ gqa_status_t current_device(int* dev, DeviceState** st) {
   *st = &s;
   return GQA_OK;
 }
+
+// Device address of the error word on the current device (looked up once
+// per device, with it current: a __device__ name in host code is only a
+// host-side stand-in).
+gqa_status_t error_word(DeviceState* st, unsigned int** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->err_word == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gqa_error_bits) != cudaSuccess || p == nullptr) return GQA_ERR_CUDA;
+    st->err_word = static_cast<unsigned int*>(p);
+  }
+  *out = st->err_word;
+  return GQA_OK;
+}
+
+#ifdef GQA_TRACE
+unsigned long long* g_trace_buf = nullptr;  // attached by gqa_trace_attach (trace builds)
+#endif
 
 // Sets the dynamic shared memory limit of a kernel once per device.
 gqa_status_t ensure_smem_attr(DeviceState* st, unsigned bit, const void* fn, int bytes) {
@@ -372,23 +398,36 @@ cudaLaunchAttribute pdl_attr(bool on) {
   return a;
 }
 
-template <int HD, int NP, bool F16>
-gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodeParams& p, cudaStream_t s) {
-  using Cfg = DecodeCfg<HD, NP>;
-  const void* fn = reinterpret_cast<const void*>(&gqa_decode_kernel<HD, NP, F16>);
-  gqa_status_t rc = ensure_smem_attr(st, attr_bit, fn, Cfg::kSmemBytes);
+KernelRef decode_kernel_ref(int head_dim, int np, bool f16, bool cluster) {
+  if (head_dim == 64) return cluster ? decode_kernel_ref_64_1(np, f16) : decode_kernel_ref_64_0(np, f16);
+  if (head_dim == 256) return cluster ? decode_kernel_ref_256_1(np, f16) : decode_kernel_ref_256_0(np, f16);
+  return cluster ? decode_kernel_ref_128_1(np, f16) : decode_kernel_ref_128_0(np, f16);
+}
+
+gqa_status_t launch_decode(DeviceState* st, DecodeParams& p, bool in_f16, cudaStream_t s) {
+  const int np = p.nq * p.G <= 16 ? 16 : 32;
+  const bool cluster = p.cluster_k > 1;
+  const KernelRef k = decode_kernel_ref(p.head_dim, np, in_f16, cluster);
+  // one attribute bit per instantiation: head_dim x columns x input type x merge mode
+  const unsigned bit = (p.head_dim == 64 ? 0u : p.head_dim == 128 ? 1u : 2u) * 8u + (np == 16 ? 0u : 4u) +
+                       (in_f16 ? 2u : 0u) + (cluster ? 1u : 0u);
+  gqa_status_t rc = ensure_smem_attr(st, bit, k.fn, k.smem_bytes);
   if (rc != GQA_OK) return rc;
+  if ((rc = error_word(st, &p.err_word)) != GQA_OK) return rc;
+#ifdef GQA_TRACE
+  p.trace_buf = g_trace_buf;
+#endif
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(static_cast<unsigned>(p.plan.num_ctas), 1, 1);
-  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.blockDim = dim3(static_cast<unsigned>(k.threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(k.smem_bytes);
   cfg.stream = s;
   cudaLaunchAttribute attrs[2];
   attrs[0] = pdl_attr(!env_flag("GQA_DISABLE_PDL"));
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  if (p.cluster_k > 1) {
+  if (cluster) {
     std::memset(&attrs[1], 0, sizeof attrs[1]);
     attrs[1].id = cudaLaunchAttributeClusterDimension;
     attrs[1].val.clusterDim.x = static_cast<unsigned>(p.cluster_k);
@@ -396,25 +435,9 @@ gqa_status_t launch_decode_t(DeviceState* st, unsigned attr_bit, const DecodePar
     attrs[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  if (cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HD, NP, F16>, p) != cudaSuccess) return GQA_ERR_CUDA;
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&cfg, k.fn, args) != cudaSuccess) return GQA_ERR_CUDA;
   return GQA_OK;
-}
-
-template <bool F16>
-gqa_status_t launch_decode_dt(DeviceState* st, const DecodeParams& p, cudaStream_t s) {
-  const int nv = p.nq * p.G;
-  const unsigned b = F16 ? 6u : 0u;
-  if (p.head_dim == 64) {
-    return nv <= 16 ? launch_decode_t<64, 16, F16>(st, b + 0, p, s) : launch_decode_t<64, 32, F16>(st, b + 1, p, s);
-  }
-  if (p.head_dim == 256) {
-    return nv <= 16 ? launch_decode_t<256, 16, F16>(st, b + 4, p, s) : launch_decode_t<256, 32, F16>(st, b + 5, p, s);
-  }
-  return nv <= 16 ? launch_decode_t<128, 16, F16>(st, b + 2, p, s) : launch_decode_t<128, 32, F16>(st, b + 3, p, s);
-}
-
-gqa_status_t launch_decode(DeviceState* st, const DecodeParams& p, bool in_f16, cudaStream_t s) {
-  return in_f16 ? launch_decode_dt<true>(st, p, s) : launch_decode_dt<false>(st, p, s);
 }
 
 gqa_status_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t s) {
@@ -748,8 +771,8 @@ gqa_status_t gqa_decode_plan(const gqa_desc_t* desc, const int32_t* seqlens_host
 // Trace builds only: attaches a device buffer of grid x TR_EVENTS x
 // kTraceBlocks uint64 for the decode kernel's event stamps (NULL detaches).
 gqa_status_t gqa_trace_attach(void* device_buffer) {
-  unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
-  return cudaMemcpyToSymbol(g_gqa_trace_buf, &p, sizeof p) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  g_trace_buf = static_cast<unsigned long long*>(device_buffer);  // used by the following launches
+  return GQA_OK;
 }
 #endif
 

@@ -104,10 +104,15 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t ran
   return d;
 }
 
-// Every thread of every CTA of the cluster (warp-converged) arrives, then
-// waits for all of them: a hardware barrier, as __syncthreads is for a CTA.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// The cluster's hardware barrier, in two halves: every thread of every CTA
+// of the cluster (warp-converged) arrives once, with release semantics, and
+// a thread that must see the others' earlier writes (barrier
+// initialisation) waits, with acquire semantics, before it relies on them.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_acq_rel_cluster() {

@@ -74,7 +74,7 @@ def test_static_workspace_matches_caller_workspace_on_consecutive_calls():
         else:
             cfg = workloads.CONFIGS[name]
             inp = workloads.make_inputs(cfg).to(DEV)
-        need = g.gqa_decode_workspace_size(inp.q, inp.k_cache, splits, causal=cfg.causal)
+        need = g.gqa_decode_workspace_size(inp.q, inp.k_cache, splits, causal=cfg.causal, reduction="combine")
         assert 0 < need <= STATIC_BYTES
         ref_out, ref_lse = _with_caller_workspace(inp, splits, cfg.causal, torch.bfloat16)
         out = torch.full_like(ref_out, float("nan"))
@@ -97,7 +97,7 @@ def test_static_workspace_refuses_problems_larger_than_it():
     k = torch.randn(B, s_max, Hkv, d, device=DEV).to(torch.bfloat16)
     sl = torch.full((B,), s_max, dtype=torch.int32, device=DEV)
     inp = workloads.DecodeInputs(None, q, k, k, sl, 0.0)
-    assert g.gqa_decode_workspace_size(q, k, 64) > STATIC_BYTES
+    assert g.gqa_decode_workspace_size(q, k, 64, reduction="combine") > STATIC_BYTES
     out = torch.full((B, 1, Hq, d), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.full((B, 1, Hq), float("nan"), device=DEV)
     assert _static_call(inp, out, lse, 64, False) == g.GQA_ERR_WORKSPACE
