@@ -167,9 +167,9 @@ struct DecodeCfg {
   static constexpr int kListBytes = 16 + kMaxListItems * static_cast<int>(sizeof(WorkItem));
   static constexpr int kMiscBytes =
       (512 + kXchgBytes + 4 * kMaxSmemB + 4 * (kMaxSmemB + 1) + 64 + kListBytes + 127) / 128 * 128;
-  // output staging, two buffers: one item's rows (fp32 worst case), its LSEs,
-  // its piece count
-  static constexpr int kOutBytes = (NPAD * HEAD_DIM * 4 + 128 + 16 + 127) / 128 * 128;
+  // output staging, two buffers: one item's rows (fp32 worst case), its LSEs
+  // (in-cluster merge: those of every CTA of the cluster), its piece count
+  static constexpr int kOutBytes = (NPAD * HEAD_DIM * 4 + kMaxClusterK * NPAD * 4 + 16 + 127) / 128 * 128;
   // in-cluster merge: this CTA's merged columns of an item (at most half of
   // d, fp32, per row), then the merged LSEs
   static constexpr int kFinBytes = (NPAD * HEAD_DIM * 2 + NPAD * 4 + 127) / 128 * 128;
@@ -318,7 +318,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // output staging buffer ob: rows, then 32 LSEs, then the piece count
   auto obuf_of = [&](int ob) -> uint8_t* { return misc + Cfg::kMiscBytes + ob * Cfg::kOutBytes; };
   auto lse_of = [&](int ob) -> float* { return reinterpret_cast<float*>(obuf_of(ob) + NPAD * HEAD_DIM * 4); };
-  auto np_of = [&](int ob) -> int32_t* { return reinterpret_cast<int32_t*>(lse_of(ob) + 32); };
+  auto np_of = [&](int ob) -> int32_t* { return reinterpret_cast<int32_t*>(lse_of(ob) + kMaxClusterK * NPAD); };
   float* xo_buf = reinterpret_cast<float*>(obuf_of(0) + NB * Cfg::kOutBytes);  // kXoBytes
   uint8_t* fin_buf = obuf_of(0) + NB * Cfg::kOutBytes + Cfg::kXoBytes;         // kFinBytes
   constexpr bool cluster_merge = CLUSTER;
@@ -343,8 +343,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // (PLAN_READY), and the rest allocate TMEM and zero the padding of the MMA
   // operand buffers.
   const int PLAN_READY = DRAIN + 2, OUT_FULL = DRAIN + 3, OUT_EMPTY = DRAIN + 5, PRE_READY = DRAIN + 7;
-  // in-cluster merge, per softmax warpgroup and staging buffer: all k CTAs
-  // have staged the warpgroup's rows (PEER_FULL) / have read them (PEER_EMPTY)
+  // in-cluster merge, per softmax warpgroup and staging buffer: the k CTAs'
+  // pieces of this CTA's columns have landed here (PEER_FULL, transaction
+  // bytes) / every CTA has merged what this CTA sent it (PEER_EMPTY)
   const int PEER_FULL = DRAIN + 8, PEER_EMPTY = DRAIN + 8 + 2 * NWG;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -369,8 +370,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     if (cluster_merge) {
       for (int i = 0; i < 2 * NWG; ++i) {
+        ptx::mbar_init(BAR(PEER_FULL + i), 1u);  // the local expect-tx arrival; the bytes come from st.async
         // one arrival per warp of the warpgroup in every CTA of the cluster
-        ptx::mbar_init(BAR(PEER_FULL + i), 4u * static_cast<uint32_t>(p.cluster_k));
         ptx::mbar_init(BAR(PEER_EMPTY + i), 4u * static_cast<uint32_t>(p.cluster_k));
       }
     }
@@ -904,7 +905,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     auto wait_staging = [&]() -> bool {
       if (threadIdx.x != sm0) return true;
       if constexpr (cluster_merge) {
-        // every CTA of the cluster has read this buffer's rows of the item two before
+        // every CTA has merged what this one sent into its buffer NB items before
         if (k_out < NB) return true;
         return ptx::mbar_wait_cluster_bounded(BAR(PEER_EMPTY + 2 * wg + static_cast<int>(k_out % NB)),
                                               ((k_out / NB) & 1u) ^ 1u, abort_flag, p.timeout_ns);
@@ -918,78 +919,86 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
                                       p.timeout_ns);
       }
     };
-    // In-cluster merge of an item (cluster_k > 1; "Building a Faster GQA
-    // Decode Kernel for Blackwell SM100", section "Reducing inside a thread
-    // block cluster", with a fixed-order sum in place of the page's
-    // reduce-add into a zeroed output).  Every CTA of the cluster has staged
-    // its piece's normalised fp32 rows and LSEs; this warpgroup's rows are
-    // exchanged through distributed shared memory, and CTA j merges columns
-    // [j d/k, (j+1) d/k) of them -- M = max_s lse_s, w_s = exp(lse_s - M),
-    // O = sum_s w_s O_s / sum_s w_s in split order s = 0..k-1, empty pieces
-    // (lse = -inf) skipped -- and writes them out; CTA 0 writes the LSEs.
-    // Each warp signals its own staged rows and its own finished reads (the
-    // barriers count 4k arrivals), so no warpgroup barrier sits on the path.
-    // A wait that runs out sets the error word; the merge then carries on
-    // (its outputs are invalid) so that every warp still reaches the
-    // warpgroup's barriers.
+    // In-cluster merge (CLUSTER; "Building a Faster GQA Decode Kernel for
+    // Blackwell SM100", section "Reducing inside a thread block cluster",
+    // with a fixed-order sum in place of the page's reduce-add into a zeroed
+    // output).  CTA j of a cluster of k owns output columns [j d/k, (j+1) d/k)
+    // of the pair.  Each CTA sends the normalised fp32 rows of its piece, and
+    // their LSEs, straight into the owners' shared memory (send_piece: st.async
+    // completing on the owner's PEER_FULL barrier), laid out [piece][column]
+    // [row] with the LSEs [piece][row].  The owner then merges locally --
+    // M = max_s lse_s, w_s = exp(lse_s - M), O = sum_s w_s O_s / sum_s w_s
+    // in piece order s = 0..k-1, empty pieces (lse = -inf) skipped -- writes
+    // its columns out (CTA 0 also the LSEs) and tells every sender, per warp,
+    // that its buffer is free again (PEER_EMPTY).  A wait that runs out sets
+    // the error word; the merge then carries on (its outputs are invalid) so
+    // that every warp still reaches the warpgroup's barriers.
+    auto send_piece = [&](const float* vals, int dr, bool with_lse, float lse_val) {
+      // vals: this thread's NC values of O row dr (columns c0 .. c0 + NC)
+      const uint32_t kc = static_cast<uint32_t>(p.cluster_k);
+      const uint32_t crank = ptx::cluster_ctarank();
+      const int dk = HEAD_DIM / static_cast<int>(kc);
+      const int ob = static_cast<int>(k_out % NB);
+      const uint32_t full_bar = BAR(PEER_FULL + 2 * wg + ob);
+      const uint32_t j = static_cast<uint32_t>(dr / dk);
+      const int c = dr - static_cast<int>(j) * dk;
+      const uint32_t dst = ptx::map_shared_rank(
+          ptx::smem_u32(obuf_of(ob)) + static_cast<uint32_t>(((static_cast<int>(crank) * dk + c) * NPAD + c0) * 4), j);
+      const uint32_t rbar = ptx::map_shared_rank(full_bar, j);
+#pragma unroll
+      for (int q = 0; q < NC / 4; ++q)
+        ptx::st_async_v4(dst + 16u * q, make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]),
+                         rbar);
+      if (with_lse) {  // this thread holds column dr's LSE (dr in [c0, c0 + NC)): to every CTA
+        const uint32_t l_loc = ptx::smem_u32(lse_of(ob) + static_cast<int>(crank) * NPAD + dr);
+        for (uint32_t s2 = 0; s2 < kc; ++s2)
+          ptx::st_async_f32(ptx::map_shared_rank(l_loc, s2), lse_val, ptx::map_shared_rank(full_bar, s2));
+      }
+    };
+
     auto cluster_merge_item = [&](const WorkItem& wi, bool last_item) {
       const uint32_t kc = static_cast<uint32_t>(p.cluster_k);
       const uint32_t crank = ptx::cluster_ctarank();
       const int ob = static_cast<int>(k_out % NB);
       const uint32_t full_bar = BAR(PEER_FULL + 2 * wg + ob);
       const uint32_t empty_bar = BAR(PEER_EMPTY + 2 * wg + ob);
-      if (!cluster_waited) {  // every CTA's barriers are initialised
-        ptx::cluster_wait();
-        cluster_waited = true;
-      }
-      __syncwarp();  // this warp's rows are staged
-      if (lane == 0)
-        for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(full_bar, s2));
+      const int dk = HEAD_DIM / static_cast<int>(kc);  // output columns of this CTA
+      // bytes every CTA sends this warpgroup: its rows of these columns and their LSEs
+      if (threadIdx.x == sm0)
+        ptx::mbar_arrive_expect_tx(full_bar, kc * static_cast<uint32_t>(dk * NC * 4 + NC * 4));
       if (!ptx::mbar_wait_cluster_bounded(full_bar, (k_out / NB) & 1u, abort_flag, p.timeout_ns))
         detail::set_error(p.err_word, kErrTimeout, abort_flag);
       if (!last_item && threadIdx.x == sm0) ptx::bulk_wait_read_all();  // earlier copies have read fin
       if (!last_item) ptx::named_barrier_sync(xbar, 128);                 // ... before fin is rewritten
 
       constexpr float kLog2e = 1.4426950408889634f;
-      const int dk = HEAD_DIM / static_cast<int>(kc);  // output columns of this CTA
-      const int ncv = dk >> 2;                         // 4-column groups per row
+      const int ncv = dk >> 2;  // 4-column groups per row
       const bool out16 = p.out_dtype != kOutF32;
+      const float* recv = reinterpret_cast<const float*>(obuf_of(ob));  // [piece][column][row]
+      const float* recv_lse = lse_of(ob);                                // [piece][row]
       uint8_t* fin_w = fin_buf + wg * (NC * HEAD_DIM * 2);
       float* fin_lse = reinterpret_cast<float*>(fin_buf + NPAD * HEAD_DIM * 2);
       // one (row, 4-column group) per thread and pass: NC rows x d / (4k) groups
       for (int tw = static_cast<int>(threadIdx.x) - sm0; tw < NC * ncv; tw += 128) {
         const int n = c0 + tw / ncv, cg = tw - (tw / ncv) * ncv;
         if (n >= nv) continue;
-        const int col = static_cast<int>(crank) * dk + cg * 4;
-        const uint32_t o_loc = ptx::smem_u32(obuf_of(ob)) + static_cast<uint32_t>((n * HEAD_DIM + col) * 4);
-        const uint32_t l_loc = ptx::smem_u32(lse_of(ob) + n);
-        // every piece's LSE in one round trip, then the rows two at a time
-        float ls[kMaxClusterK];
-#pragma unroll
-        for (int s2 = 0; s2 < kMaxClusterK; ++s2)
-          ls[s2] = s2 < static_cast<int>(kc) ? ptx::ld_cluster_f32(ptx::map_shared_rank(l_loc, static_cast<uint32_t>(s2)))
-                                             : -INFINITY;
         float M = -INFINITY;
 #pragma unroll
-        for (int s2 = 0; s2 < kMaxClusterK; ++s2) M = fmaxf(M, ls[s2]);
+        for (int s2 = 0; s2 < kMaxClusterK; ++s2)
+          if (s2 < static_cast<int>(kc)) M = fmaxf(M, recv_lse[s2 * NPAD + n]);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float lse_out = -INFINITY;
         if (M != -INFINITY) {
           float W = 0.f;
 #pragma unroll
-          for (int s2 = 0; s2 < kMaxClusterK; s2 += 2) {
-            if (s2 < static_cast<int>(kc)) {  // kc is a power of two >= 2: pieces s2 and s2 + 1
-              const float4 oa = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, static_cast<uint32_t>(s2)));
-              const float4 o2 = ptx::ld_cluster_v4(ptx::map_shared_rank(o_loc, static_cast<uint32_t>(s2 + 1)));
-              const float wa = ls[s2] == -INFINITY ? 0.f : ptx::ex2_approx((ls[s2] - M) * kLog2e);
-              const float wb = ls[s2 + 1] == -INFINITY ? 0.f : ptx::ex2_approx((ls[s2 + 1] - M) * kLog2e);
-              W += wa;
-              if (wa != 0.f) {
-                acc.x += wa * oa.x; acc.y += wa * oa.y; acc.z += wa * oa.z; acc.w += wa * oa.w;
-              }
-              W += wb;
-              if (wb != 0.f) {
-                acc.x += wb * o2.x; acc.y += wb * o2.y; acc.z += wb * o2.z; acc.w += wb * o2.w;
+          for (int s2 = 0; s2 < kMaxClusterK; ++s2) {
+            if (s2 < static_cast<int>(kc)) {
+              const float l2 = recv_lse[s2 * NPAD + n];
+              const float w = l2 == -INFINITY ? 0.f : ptx::ex2_approx((l2 - M) * kLog2e);
+              W += w;
+              if (w != 0.f) {
+                const float* o2 = recv + (s2 * dk + cg * 4) * NPAD + n;
+                acc.x += w * o2[0]; acc.y += w * o2[NPAD]; acc.z += w * o2[2 * NPAD]; acc.w += w * o2[3 * NPAD];
               }
             }
           }
@@ -997,6 +1006,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
           lse_out = M + 0.69314718055994531f * __log2f(W);
         }
+        const int col = static_cast<int>(crank) * dk + cg * 4;
         const int t = n / p.G;
         const long long grow =
             (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G + (n - t * p.G);
@@ -1025,7 +1035,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           if (crank == 0 && cg == 0) fin_lse[n] = lse_out;
         }
       }
-      __syncwarp();  // this warp's reads of the other CTAs' rows are done
+      __syncwarp();  // this warp's reads of the received pieces are done
       if (lane == 0)
         for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(empty_bar, s2));
       if (!last_item) {
@@ -1093,6 +1103,18 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         // empty item: final output O = 0, lse = -inf; partial lse = -inf
         const bool st_ok = wait_staging();
         if (exchange(st_ok ? 0u : 2u, false, 0.f) & 2u) { aborted = true; break; }
+        if constexpr (cluster_merge) {
+          if (!cluster_waited) {  // every CTA's barriers are initialised
+            ptx::cluster_wait();
+            cluster_waited = true;
+          }
+          float zeros[NC];
+#pragma unroll
+          for (int n = 0; n < NC; ++n) zeros[n] = 0.f;
+          for (int dr = r; dr < HEAD_DIM; dr += 128) send_piece(zeros, dr, dr >= c0 && dr < c0 + NC, -INFINITY);
+          if (!hand_over(it, !iter.has_next())) { aborted = true; break; }
+          continue;
+        }
         uint8_t* ob = obuf_of(static_cast<int>(k_out % NB));
         for (int dr = r; dr < HEAD_DIM; dr += 128) {  // rows r (and r + 128 for head_dim 256)
           for (int n = c0; n < c0 + NC && n < nv; ++n) {
@@ -1342,6 +1364,30 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         ptx::named_barrier_sync(xbar, 128);  // xo is read before P is rewritten
         writer = r < 64;
       }
+      constexpr int kRowsOut = HEAD_DIM == 256 ? 2 : 1;  // O rows of this thread: r (+ 128)
+      if constexpr (cluster_merge) {
+        // the piece's rows go to the CTAs owning their columns
+        if (!cluster_waited) {  // every CTA's barriers are initialised
+          ptx::cluster_wait();
+          cluster_waited = true;
+        }
+        if (writer) {
+          float inv[NC];
+#pragma unroll
+          for (int n = 0; n < NC; ++n) inv[n] = lt[n] > 0.f ? ptx::rcp_approx(lt[n]) : 0.f;
+          float lse_d = -INFINITY;  // the LSE of column d_row, when this thread holds it
+#pragma unroll
+          for (int n = 0; n < NC; ++n)
+            if (c0 + n == d_row && lt[n] > 0.f) lse_d = 0.69314718055994531f * (m[n] + __log2f(lt[n]));
+#pragma unroll
+          for (int h2 = 0; h2 < kRowsOut; ++h2) {
+            float vals[NC];
+#pragma unroll
+            for (int n = 0; n < NC; ++n) vals[n] = o[h2 * NC + n] * inv[n];
+            send_piece(vals, d_row + 128 * h2, h2 == 0 && d_row >= c0 && d_row < c0 + NC, lse_d);
+          }
+        }
+      } else
       // Outputs go to shared memory in their global layout (row n = t*G + g
       // of this pair, d contiguous); the output warp writes them out.
       if (writer) {
@@ -1349,7 +1395,6 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         // input type
         const bool out16 = it.slot < 0 && p.out_dtype != kOutF32;
         uint8_t* obuf = obuf_of(static_cast<int>(k_out % NB));
-        constexpr int kRowsOut = HEAD_DIM == 256 ? 2 : 1;  // O rows of this thread: r (+ 128)
 #pragma unroll
         for (int n = 0; n < NC; ++n) {
           const float inv = lt[n] > 0.f ? ptx::rcp_approx(lt[n]) : 0.f;
@@ -1385,8 +1430,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (threadIdx.x == kSoftmaxThread0) ptx::bulk_wait_all();  // this CTA's outputs are in global memory
     }
     if (cluster_merge && threadIdx.x == sm0) {
-      // The other CTAs read this CTA's staging buffers until they arrive on
-      // PEER_EMPTY: the CTA may not exit before (bounded waits).
+      // Every CTA this one sent pieces to has merged them (so the stores have
+      // landed) once it arrives on PEER_EMPTY: wait before exiting (bounded).
       for (uint32_t i = k_out >= NB ? k_out - NB : 0u; i < k_out; ++i)
         ptx::mbar_wait_cluster_bounded(BAR(PEER_EMPTY + 2 * wg + static_cast<int>(i % NB)), (i / NB) & 1u,
                                        abort_flag, p.timeout_ns);

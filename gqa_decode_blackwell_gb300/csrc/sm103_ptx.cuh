@@ -153,6 +153,19 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
   }
 }
 
+// Asynchronous stores into another CTA's shared memory (cluster-window
+// addresses) that complete on that CTA's mbarrier (its cluster-window
+// address) with the stored bytes as transaction count: the data is visible
+// to threads that observe the barrier's phase complete.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar) : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t dst, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+               ::"r"(dst), "f"(v), "r"(remote_bar) : "memory");
+}
+
 // Loads from another CTA's shared memory (cluster-window addresses).
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   float v;
