@@ -178,11 +178,21 @@ constexpr int kItemUnits32 = 3;
 
 // Cluster size of the in-cluster merge ("Building a Faster GQA Decode Kernel
 // for Blackwell SM100", section "Reducing inside a thread block cluster":
-// the KV splits of one batch entry and head group form a cluster; automatic
-// selection takes it for at most four splits, or eight with at most 64 CTAs).
-// Returns 0 when the kernel-reduction plans (combine launch) are to be used,
-// else the number k >= 1 of splits per pair, and -1 for a forced in-cluster
-// merge that cannot be done (a split count that is not a power of two <= 8).
+// the KV splits of one batch entry and head group form a cluster; the page's
+// automatic selection takes it for at most four splits, or eight with at
+// most 64 CTAs).  Returns 0 when the kernel-reduction plans (combine launch)
+// are to be used, else the number k >= 1 of splits per pair, and -1 for a
+// forced in-cluster merge that cannot be done (a split count that is not a
+// power of two <= 8).
+//
+// The automatic choice keeps the page's limits and adds what a sweep on
+// GB300 showed (CUDA graphs, pool > L2, per call, cluster minus the best
+// combine plan): grids of 128 CTAs with k = 2 gained 0.3-0.8 us and a
+// library-chosen split count gained up to 1.5 us where the balanced plan cuts
+// few pairs very finely; every grid below 64 CTAs lost 0.3-1.1 us (a cluster
+// of 4 CTAs: 7.82 against 7.14 us), explicit split counts 4 and 8 lost
+// 0.3-1.1 us against the fixed-split plan, and 16 clusters of 8 took twice
+// as long (they do not all fit on the GPU at once).
 int cluster_splits(const gqa_desc_t* d, int num_splits, int sm, bool force_partial) {
   if (force_partial || d->reduction == GQA_REDUCE_COMBINE) return 0;
   const bool forced = d->reduction == GQA_REDUCE_CLUSTER;
@@ -194,16 +204,17 @@ int cluster_splits(const gqa_desc_t* d, int num_splits, int sm, bool force_parti
     const long long lim = per_pair < nblk_cap ? per_pair : nblk_cap;
     const int k = lim >= 1 ? pow2_floor_k(lim) : 1;
     if (forced) return k;
-    // Only where the cluster grid keeps at least half the CTAs of the
-    // automatic balanced plan (k whole CTAs per pair, or one per block):
+    // Only where a cluster CTA streams at most 3 blocks more than a CTA of
+    // the automatic balanced plan (k whole CTAs per pair, or one per block):
     // one long pair, say, is spread over every SM there, not over 8.
     const long long bal_ctas = per_pair * pairs < pairs * nblk_cap ? per_pair * pairs : pairs * nblk_cap;
+    const long long extra = (nblk_cap + k - 1) / k - (pairs * nblk_cap + bal_ctas - 1) / bal_ctas;
     const bool short_seqs = nblk_cap <= 32 * k;
-    return (k >= 2 && short_seqs && 2 * k * pairs >= bal_ctas && (k <= 4 || pairs * k <= 64)) ? k : 0;
+    return (k >= 2 && short_seqs && extra <= 3 && (k <= 4 || pairs * k <= 64) && k * pairs >= 64) ? k : 0;
   }
   const bool pow2 = (num_splits & (num_splits - 1)) == 0;
   if (forced) return (pow2 && num_splits <= kMaxClusterK) ? num_splits : -1;
-  return (num_splits >= 2 && pow2 && (num_splits <= 4 || (num_splits == 8 && pairs * 8 <= 64))) ? num_splits : 0;
+  return (num_splits == 2 && pairs * 2 >= 128) ? 2 : 0;
 }
 
 HostPlan make_plan(const gqa_desc_t* d, int num_splits, int sm, bool force_partial) {

@@ -73,12 +73,15 @@ typedef enum { GQA_DTYPE_BF16 = 0, GQA_DTYPE_FP32 = 1, GQA_DTYPE_FP16 = 2 } gqa_
  *                       a power of two <= 8 (num_splits = 0: the largest
  *                       power of two <= min(8, #SMs / pairs, blocks));
  *                       otherwise GQA_ERR_UNSUPPORTED;
- *   GQA_REDUCE_AUTO     the page's selection: the in-cluster merge for at most
- *                       four splits, or eight with at most 64 CTAs; with
- *                       num_splits = 0, when the automatic plan would give
- *                       every pair k >= 2 whole CTAs of at most 32 blocks
- *                       each (short sequences) and the k * pairs CTAs are at
- *                       least half of that plan's, else the combine kernel. */
+ *   GQA_REDUCE_AUTO     the page's selection (at most four splits, or eight
+ *                       with at most 64 CTAs) narrowed by measurement on
+ *                       GB300: with num_splits = 0, the in-cluster merge when
+ *                       the automatic plan would give every pair k >= 2 whole
+ *                       CTAs of at most 32 blocks each (short sequences), the
+ *                       k * pairs CTAs are at least 64 and each streams at
+ *                       most 3 blocks more than one of that plan's; with an
+ *                       explicit count, for 2 splits on
+ *                       at least 128 CTAs; otherwise the combine kernel. */
 typedef enum { GQA_REDUCE_AUTO = 0, GQA_REDUCE_COMBINE = 1, GQA_REDUCE_CLUSTER = 2 } gqa_reduction_t;
 
 /* Problem description.  Q is [batch, q_tokens, q_heads, head_dim]; the K

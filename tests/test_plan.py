@@ -205,16 +205,18 @@ def test_balanced_plan_needs_int32_prefix_sums():
 def _cluster_k_auto(pairs, sm, s_max):
     """The automatic choice: k = the largest power of two <= min(8, sm // pairs,
     blocks), taken when k >= 2, the cache spans at most 32 k blocks, the k *
-    pairs CTAs are at least half of the balanced plan's (sm // pairs per pair,
-    at most one per block), and k <= 4 or k * pairs <= 64; else 0 (the
-    combine kernel)."""
+    pairs CTAs are at least 64, each streams at most 3 blocks more than a CTA
+    of the balanced plan (sm // pairs per pair, at most one per block), and
+    k <= 4 or k * pairs <= 64; else 0 (the combine kernel)."""
     per_pair = sm // pairs
     lim = min(per_pair, _blocks(s_max))
     k = 1
     while 2 * k <= lim and k < 8:
         k *= 2
-    bal = min(per_pair * pairs, pairs * _blocks(s_max))
-    if k >= 2 and _blocks(s_max) <= 32 * k and 2 * k * pairs >= bal and (k <= 4 or pairs * k <= 64):
+    nb = _blocks(s_max)
+    bal = min(per_pair * pairs, pairs * nb)
+    extra = -(-nb // k) - (-(-pairs * nb // bal))
+    if k >= 2 and nb <= 32 * k and extra <= 3 and (k <= 4 or pairs * k <= 64) and k * pairs >= 64:
         return k
     return 0
 
@@ -248,8 +250,8 @@ def check_cluster(lens, Hkv, s_max, sm, k, G=4, nq=1, num_splits=0, reduction=g.
 @pytest.mark.parametrize("B,Hkv,L,G,nq,k", [
     (8, 8, 4096, 4, 1, 2),      # Llama-8B-shaped: 64 pairs, clusters of two
     (32, 2, 2048, 8, 4, 2),     # speculative
-    (1, 1, 512, 8, 1, 4),       # tiny: four blocks, a cluster of four
     (8, 1, 1024, 4, 1, 8),      # 8 pairs x 8 <= 64 CTAs, 8 blocks each
+    (1, 8, 4096, 4, 1, 8),      # 8 pairs x 8 = 64 CTAs
     (4, 8, 8192, 8, 1, 4),      # 32 pairs, 64 blocks <= 32 x 4
 ])
 def test_auto_selects_cluster_merge_for_short_sequences(B, Hkv, L, G, nq, k):
@@ -263,6 +265,7 @@ def test_auto_selects_cluster_merge_for_short_sequences(B, Hkv, L, G, nq, k):
     (1, 1, 65536, 4, 1, 1),     # one long sequence
     (1, 1, 32768, 4, 1, 1),     # one pair: 8 CTAs would be far fewer than the balanced plan's 152
     (1, 2, 4096, 4, 1, 1),      # 2 pairs: 16 CTAs against 64
+    (1, 1, 512, 8, 1, 1),       # tiny: a cluster of 4 CTAs is below 64
 ])
 def test_auto_keeps_combine_for_long_sequences_or_many_pairs(B, Hkv, L, G, nq, mode):
     assert _cluster_k_auto(B * Hkv, 152, L) == 0
@@ -272,11 +275,12 @@ def test_auto_keeps_combine_for_long_sequences_or_many_pairs(B, Hkv, L, G, nq, m
 
 
 @pytest.mark.parametrize("S,pairs,expect", [
-    (2, 64, 2), (4, 64, 4), (4, 400, 4), (8, 8, 8), (8, 9, 0), (8, 128, 0), (3, 4, 0), (16, 2, 0), (1, 4, 0),
+    (2, 64, 2), (2, 400, 2), (2, 63, 0), (2, 1, 0), (4, 64, 0), (4, 400, 0), (8, 8, 0), (8, 128, 0), (3, 4, 0),
+    (16, 2, 0), (1, 4, 0),
 ])
-def test_explicit_split_counts_follow_the_pages_selection(S, pairs, expect):
-    """At most four splits, or eight with at most 64 CTAs, merge in the
-    cluster (power-of-two counts); other counts use the combine kernel."""
+def test_explicit_split_counts_follow_the_measured_selection(S, pairs, expect):
+    """An explicit split count merges in the cluster for 2 splits on at least
+    128 CTAs (where it measured faster); other counts use the combine kernel."""
     lens = [2000] * pairs
     C, mode, slots, items = g.gqa_decode_plan(_desc(pairs, 1, 2000, reduction=g.GQA_REDUCE_AUTO), lens, S, 152)
     if expect:
