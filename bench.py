@@ -110,7 +110,7 @@ def ncu_traffic(workload: str):
     if fields.get("kernel_source_sha256") != kernel_source_digest():
         return None, "kernel changed since the ncu capture"
     try:
-        return float(fields["dram_bytes_per_launch"]), path
+        return float(fields["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
     except (KeyError, ValueError):
         return None, "summary has no dram_bytes_per_launch"
 
