@@ -496,7 +496,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="ragged", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="ragged", choices=sorted(workloads.CONFIGS) + ["all"],
+                    help="the workload; 'all' prints one JSON line for each of the five in turn")
     ap.add_argument("--len-div", type=int, default=1,
                     help="divide the workload's KV lengths by this (smaller profiling captures only)")
     ap.add_argument("--splits", type=int, default=None, help="0 = automatic (default: the config's first)")
@@ -512,13 +513,15 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")
-    cfg = workloads.CONFIGS[args.config]
-    if args.splits is None:
-        args.splits = cfg.num_splits[0]
+    names = list(workloads.CONFIG_ORDER) if args.config == "all" else [args.config]
+    splits_arg = args.splits
     world, rank, local = dist_env()
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(bench_reference(args, cfg)), flush=True)
+            for name in names:
+                cfg = workloads.CONFIGS[name]
+                args.splits = cfg.num_splits[0] if splits_arg is None else splits_arg
+                print(json.dumps(bench_reference(args, cfg)), flush=True)
         return 0
     if world > 1:
         import torch.distributed as dist
@@ -526,9 +529,14 @@ def main(argv=None):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     try:
-        res = bench_ours(args, cfg, world, rank, local)
-        if rank == 0:
-            print(json.dumps(res), flush=True)
+        for name in names:
+            cfg = workloads.CONFIGS[name]
+            args.splits = cfg.num_splits[0] if splits_arg is None else splits_arg
+            res = bench_ours(args, cfg, world, rank, local)
+            if rank == 0:
+                print(json.dumps(res), flush=True)
+            del res
+            torch.cuda.empty_cache()
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -24,6 +24,7 @@ GQA_ERR_WORKSPACE = 3
 GQA_ERR_CUDA = 4
 GQA_ERR_TIMEOUT = 5
 GQA_ERR_BAD_SEQLEN = 6
+GQA_ERR_BOUNDS = 7
 GQA_DTYPE_BF16 = 0
 GQA_DTYPE_FP32 = 1
 GQA_DTYPE_FP16 = 2
@@ -66,34 +67,40 @@ def lib() -> ctypes.CDLL:
             if not os.path.exists(LIB):
                 raise RuntimeError(f"GQA decode CUDA library not built ({LIB}); run "
                                    "gqa_decode_blackwell_gb300.build.build() or __graft_entry__.build()")
-            L = ctypes.CDLL(LIB)
-            P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
-            D = ctypes.POINTER(gqa_desc_t)
-            L.gqa_decode_workspace_size.argtypes = [D, I]
-            L.gqa_decode_workspace_size.restype = SZ
-            L.gqa_decode_attn.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
-            L.gqa_decode_attn.restype = I
-            L.gqa_decode_attn_static_workspace.argtypes = [D, P, P, P, P, P, P, I, P]
-            L.gqa_decode_attn_static_workspace.restype = I
-            L.gqa_decode_attn_split.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
-            L.gqa_decode_attn_split.restype = I
-            L.gqa_decode_attn_merge.argtypes = [D, P, P, I, P, SZ, P]
-            L.gqa_decode_attn_merge.restype = I
-            L.gqa_decode_splitkv.argtypes = [D, P, P, P, P, I, P, P, P]
-            L.gqa_decode_splitkv.restype = I
-            L.gqa_decode_combine.argtypes = [P, P, I, I64, I, P, I, P, P]
-            L.gqa_decode_combine.restype = I
-            L.gqa_decode_get_error.argtypes = [I]
-            L.gqa_decode_get_error.restype = I
-            L.gqa_status_string.argtypes = [I]
-            L.gqa_status_string.restype = ctypes.c_char_p
-            L.gqa_decode_plan.argtypes = [D, P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I), P,
-                                          I64, ctypes.POINTER(I64)]
-            L.gqa_decode_plan.restype = I
-            L.gqa_decode_selftest_timeout.argtypes = [ctypes.c_uint, P]
-            L.gqa_decode_selftest_timeout.restype = I
-            _lib = L
+            _lib = load_library(LIB)
         return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """A build of the C library at `path` (say the -DGQA_DEBUG one) with its
+    functions' argument and result types declared."""
+    L = ctypes.CDLL(path)
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    D = ctypes.POINTER(gqa_desc_t)
+    L.gqa_decode_workspace_size.argtypes = [D, I]
+    L.gqa_decode_workspace_size.restype = SZ
+    L.gqa_decode_attn.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
+    L.gqa_decode_attn.restype = I
+    L.gqa_decode_attn_static_workspace.argtypes = [D, P, P, P, P, P, P, I, P]
+    L.gqa_decode_attn_static_workspace.restype = I
+    L.gqa_decode_attn_split.argtypes = [D, P, P, P, P, P, P, I, P, SZ, P]
+    L.gqa_decode_attn_split.restype = I
+    L.gqa_decode_attn_merge.argtypes = [D, P, P, I, P, SZ, P]
+    L.gqa_decode_attn_merge.restype = I
+    L.gqa_decode_splitkv.argtypes = [D, P, P, P, P, I, P, P, P]
+    L.gqa_decode_splitkv.restype = I
+    L.gqa_decode_combine.argtypes = [P, P, I, I64, I, P, I, P, P]
+    L.gqa_decode_combine.restype = I
+    L.gqa_decode_get_error.argtypes = [I]
+    L.gqa_decode_get_error.restype = I
+    L.gqa_status_string.argtypes = [I]
+    L.gqa_status_string.restype = ctypes.c_char_p
+    L.gqa_decode_plan.argtypes = [D, P, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I), P,
+                                  I64, ctypes.POINTER(I64)]
+    L.gqa_decode_plan.restype = I
+    L.gqa_decode_selftest_timeout.argtypes = [ctypes.c_uint, P]
+    L.gqa_decode_selftest_timeout.restype = I
+    return L
 
 
 def header_functions():

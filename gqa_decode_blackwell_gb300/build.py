@@ -14,6 +14,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 HEADER = os.path.join(ROOT, "include", "gqa_decode.h")
 LIB = os.path.join(PKG, "libgqa_decode_sm103.so")
+# The same library with device-side bounds checks (-DGQA_DEBUG): every
+# global write of the decode kernel is checked against its buffer and
+# skipped if outside it, every TMA tile origin against its tensor; either
+# shows as GQA_ERR_BOUNDS from gqa_decode_get_error.  For testing only.
+DEBUG_LIB = os.path.join(PKG, "libgqa_decode_sm103_debug.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -70,6 +75,11 @@ def build(force: bool = False, out: str = LIB, extra_flags=(), verbose: bool = F
     subprocess.run([_nvcc(), ARCH, "-shared", *[obj for obj, _ in procs], "-o", out + ".tmp"], check=True)
     os.replace(out + ".tmp", out)
     return out
+
+
+def build_debug(force: bool = False) -> str:
+    """The -DGQA_DEBUG build of the library (bounds-checked), beside the other."""
+    return build(force=force, out=DEBUG_LIB, extra_flags=("-DGQA_DEBUG",))
 
 
 if __name__ == "__main__":

@@ -59,7 +59,7 @@
 
 namespace gqa {
 
-enum : unsigned { kErrTimeout = 1u, kErrBadSeqlen = 2u };
+enum : unsigned { kErrTimeout = 1u, kErrBadSeqlen = 2u, kErrBounds = 4u };
 
 // Optional per-CTA event trace (compile with -DGQA_TRACE): clock64 stamps of
 // each role's per-block steps, written to the buffer the host attaches with
@@ -123,8 +123,10 @@ struct DecodeParams {
   int cluster_k;      // > 1: the CTAs of a k-cluster hold the k pieces of a pair and merge them in
                       // distributed shared memory (fixed splits, k = plan.num_splits)
   unsigned long long timeout_ns;
-  unsigned int* err_word;            // the library's device error word (kErrTimeout | kErrBadSeqlen)
+  unsigned int* err_word;            // the library's device error word (kErrTimeout | kErrBadSeqlen | kErrBounds)
   unsigned long long* trace_buf;     // -DGQA_TRACE builds: [grid][TR_EVENTS][kTraceBlocks] stamps, or null
+  // byte extents of the buffers the kernel writes, checked by -DGQA_DEBUG builds
+  unsigned long long out_bytes, lse_bytes, o_part_bytes, lse_part_bytes, n_pieces_bytes;
 };
 
 template <int HEAD_DIM, int NPAD>
@@ -243,6 +245,35 @@ __device__ __forceinline__ int transpose_col(int lane) {
 __device__ __forceinline__ void set_error(unsigned int* word, unsigned bits, volatile int* abort_flag) {
   atomicOr(word, bits);
   if (abort_flag != nullptr) *abort_flag = 1;
+}
+
+// -DGQA_DEBUG builds: whether the write [dst, dst + len) lies inside the
+// buffer [base, base + bytes); a write that would not is skipped by the
+// caller and recorded in the error word (kErrBounds).  Other builds: true.
+__device__ __forceinline__ bool write_ok(unsigned int* word, const void* base, unsigned long long bytes,
+                                         const void* dst, unsigned long long len) {
+#ifdef GQA_DEBUG
+  const unsigned long long b = reinterpret_cast<unsigned long long>(base);
+  const unsigned long long d = reinterpret_cast<unsigned long long>(dst);
+  if (base == nullptr || d < b || d + len > b + bytes) {
+    atomicOr(word, kErrBounds);
+    return false;
+  }
+#else
+  (void)word; (void)base; (void)bytes; (void)dst; (void)len;
+#endif
+  return true;
+}
+
+// -DGQA_DEBUG builds: records (kErrBounds) a TMA tile origin outside its
+// tensor.  The load is still issued -- its barrier expects the bytes, and a
+// tiled load outside the tensor reads the fill value, it does not fault.
+__device__ __forceinline__ void check_coord(unsigned int* word, bool ok) {
+#ifdef GQA_DEBUG
+  if (!ok) atomicOr(word, kErrBounds);
+#else
+  (void)word; (void)ok;
+#endif
 }
 
 }  // namespace detail
@@ -603,11 +634,15 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         uint8_t* dst = final_out
             ? static_cast<uint8_t*>(p.out) + row0 * HEAD_DIM * esz
             : reinterpret_cast<uint8_t*>(p.o_part + (static_cast<long long>(wi.slot) * rows_total + row0) * HEAD_DIM);
-        ptx::bulk_store(dst, ptx::smem_u32(obuf_of(ob) + static_cast<uint32_t>(t) * row_bytes), row_bytes);
+        if (detail::write_ok(p.err_word, final_out ? p.out : static_cast<void*>(p.o_part),
+                             final_out ? p.out_bytes : p.o_part_bytes, dst, row_bytes))
+          ptx::bulk_store(dst, ptx::smem_u32(obuf_of(ob) + static_cast<uint32_t>(t) * row_bytes), row_bytes);
       }
       float* lse_dst = final_out ? (p.lse != nullptr ? p.lse + row0 : nullptr)
                                  : p.lse_part + static_cast<long long>(wi.slot) * rows_total + row0;
-      if (lse_dst != nullptr) {
+      if (lse_dst != nullptr &&
+          detail::write_ok(p.err_word, final_out ? p.lse : p.lse_part, final_out ? p.lse_bytes : p.lse_part_bytes,
+                           lse_dst, static_cast<unsigned long long>(p.G) * 4u)) {
         if (p.lse_bulk) {
           ptx::bulk_store(lse_dst, ptx::smem_u32(lse_st + t * p.G), static_cast<uint32_t>(p.G) * 4u);
         } else {
@@ -615,7 +650,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       }
     }
-    if (wi.first_piece && p.n_pieces != nullptr) {
+    if (wi.first_piece && p.n_pieces != nullptr &&
+        detail::write_ok(p.err_word, p.n_pieces, p.n_pieces_bytes, p.n_pieces + pair_idx * 4, 16u)) {
       np_of(ob)[0] = wi.n_pieces;
       ptx::fence_proxy_async_smem();
       ptx::bulk_store(p.n_pieces + pair_idx * 4, ptx::smem_u32(np_of(ob)), 16u);
@@ -645,6 +681,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
             !ptx::mbar_wait_bounded(BAR(RING_EMPTY + stage), phase ^ 1u, abort_flag, p.timeout_ns))
           return false;
         ptx::mbar_arrive_expect_tx(BAR(RING_FULL + stage), Cfg::kSlotBytes);
+        detail::check_coord(p.err_word, b >= 0 && b < plan.batch && h >= 0 && h < plan.kv_heads && blk >= 0 &&
+                                            blk * kBlockN < plan.max_seqlen && half >= 0 && half < TPB);
         uint8_t* dst = ring + stage * Cfg::kSlotBytes;
         const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
 #pragma unroll
@@ -672,6 +710,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           break;
         }
         ptx::mbar_arrive_expect_tx(BAR(Q_FULL + qb), KCH * p.nq * p.G * 128);
+        detail::check_coord(p.err_word, it.b >= 0 && it.b < plan.batch && it.h >= 0 && (it.h + 1) * p.G <= p.Hq);
 #pragma unroll
         for (int kc = 0; kc < KCH; ++kc)
           ptx::tma_load_4d(ptx::smem_u32(qbuf + qb * Cfg::kQBytes + kc * NPAD * 128), &p.tm_q,
@@ -1023,11 +1062,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         if (last_item) {
           // Nothing of this CTA is still streaming in: plain stores, straight
           // from registers (16- or 8-byte aligned: col is a multiple of 4).
-          if (out16)
-            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + grow * HEAD_DIM + col) = packed;
-          else
-            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + grow * HEAD_DIM + col) = acc;
-          if (crank == 0 && cg == 0 && p.lse != nullptr) p.lse[grow] = lse_out;
+          if (out16) {
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + grow * HEAD_DIM + col;
+            if (detail::write_ok(p.err_word, p.out, p.out_bytes, dst, 8u)) *reinterpret_cast<uint2*>(dst) = packed;
+          } else {
+            float* dst = static_cast<float*>(p.out) + grow * HEAD_DIM + col;
+            if (detail::write_ok(p.err_word, p.out, p.out_bytes, dst, 16u)) *reinterpret_cast<float4*>(dst) = acc;
+          }
+          if (crank == 0 && cg == 0 && p.lse != nullptr &&
+              detail::write_ok(p.err_word, p.lse, p.lse_bytes, p.lse + grow, 4u))
+            p.lse[grow] = lse_out;
         } else {
           const int e = (n - c0) * dk + cg * 4;  // element of this warpgroup's merged rows
           if (out16) *reinterpret_cast<uint2*>(fin_w + e * 2) = packed;
@@ -1051,8 +1095,9 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
             const int t = n2 / p.G, g2 = n2 - t * p.G;
             const long long grow =
                 (static_cast<long long>(wi.b) * p.nq + t) * p.Hq + static_cast<long long>(wi.h) * p.G + g2;
-            ptx::bulk_store(static_cast<uint8_t*>(p.out) + (grow * HEAD_DIM + static_cast<long long>(crank) * dk) * esz,
-                            ptx::smem_u32(fin_w + (n2 - c0) * slice), slice);
+            uint8_t* dst = static_cast<uint8_t*>(p.out) + (grow * HEAD_DIM + static_cast<long long>(crank) * dk) * esz;
+            if (detail::write_ok(p.err_word, p.out, p.out_bytes, dst, slice))
+              ptx::bulk_store(dst, ptx::smem_u32(fin_w + (n2 - c0) * slice), slice);
           }
           if (crank == 0 && p.lse != nullptr) {
             // runs of rows of one query token are contiguous in lse
@@ -1061,7 +1106,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
               const int run_end = (t + 1) * p.G < n_end ? (t + 1) * p.G : n_end;
               const long long grow = (static_cast<long long>(wi.b) * p.nq + t) * p.Hq +
                                      static_cast<long long>(wi.h) * p.G + (n2 - t * p.G);
-              if (p.lse_bulk) {
+              if (!detail::write_ok(p.err_word, p.lse, p.lse_bytes, p.lse + grow,
+                                    static_cast<unsigned long long>(run_end - n2) * 4u)) {
+                // outside lse: skipped (debug builds)
+              } else if (p.lse_bulk) {
                 ptx::bulk_store(p.lse + grow, ptx::smem_u32(fin_lse + n2), static_cast<uint32_t>(run_end - n2) * 4u);
               } else {
                 for (int i = n2; i < run_end; ++i) p.lse[grow + (i - n2)] = fin_lse[i];

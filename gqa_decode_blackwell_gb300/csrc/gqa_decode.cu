@@ -564,6 +564,12 @@ gqa_status_t attn_impl(const gqa_desc_t* desc, const void* q, const void* k_cach
     p.o_part = o_part;
     p.lse_part = lse_part;
     p.n_pieces = n_pieces;
+    const size_t rows = static_cast<size_t>(desc->batch) * desc->q_tokens * desc->q_heads;
+    p.out_bytes = rows * desc->head_dim * (desc->out_dtype == GQA_DTYPE_FP32 ? 4u : 2u);
+    p.lse_bytes = lse != nullptr ? rows * 4u : 0u;
+    p.o_part_bytes = hp.combine ? wl.lse_off - wl.o_off : 0u;
+    p.lse_part_bytes = hp.combine ? wl.np_off - wl.lse_off : 0u;
+    p.n_pieces_bytes = (hp.combine && hp.use_n_pieces) ? wl.total - wl.np_off : 0u;
     if ((rc = launch_decode(st, p, desc->in_dtype == GQA_DTYPE_FP16, s)) != GQA_OK) return rc;
   }
   if (!(parts & ATTN_MERGE) || !hp.combine) return GQA_OK;
@@ -681,6 +687,9 @@ gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const voi
   if ((rc = prepare_decode(desc, q, k_cache, v_cache, seqlens, hp, &p)) != GQA_OK) return rc;
   p.o_part = o_part;
   p.lse_part = lse_part;
+  const size_t rows = static_cast<size_t>(desc->batch) * desc->q_tokens * desc->q_heads;
+  p.o_part_bytes = static_cast<size_t>(num_splits) * rows * desc->head_dim * 4u;
+  p.lse_part_bytes = static_cast<size_t>(num_splits) * rows * 4u;
   return launch_decode(st, p, desc->in_dtype == GQA_DTYPE_FP16, static_cast<cudaStream_t>(stream));
 }
 
@@ -716,6 +725,7 @@ gqa_status_t gqa_decode_get_error(int clear) {
     if (cudaMemcpyToSymbol(g_gqa_error_bits, &zero, sizeof zero) != cudaSuccess) return GQA_ERR_CUDA;
   }
   if (bits & kErrTimeout) return GQA_ERR_TIMEOUT;
+  if (bits & kErrBounds) return GQA_ERR_BOUNDS;
   if (bits & kErrBadSeqlen) return GQA_ERR_BAD_SEQLEN;
   return GQA_OK;
 }
@@ -729,6 +739,7 @@ const char* gqa_status_string(gqa_status_t status) {
     case GQA_ERR_CUDA: return "CUDA runtime error";
     case GQA_ERR_TIMEOUT: return "a kernel wait timed out";
     case GQA_ERR_BAD_SEQLEN: return "sequence length out of range (clamped)";
+    case GQA_ERR_BOUNDS: return "a write or tile outside its buffer was caught (debug build)";
   }
   return "unknown status";
 }

@@ -54,7 +54,9 @@ typedef enum {
   GQA_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small */
   GQA_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute) */
   GQA_ERR_TIMEOUT = 5,      /* a kernel wait ran out (see gqa_decode_get_error) */
-  GQA_ERR_BAD_SEQLEN = 6    /* a sequence length was < 0 or > max_seqlen */
+  GQA_ERR_BAD_SEQLEN = 6,   /* a sequence length was < 0 or > max_seqlen */
+  GQA_ERR_BOUNDS = 7        /* library built with -DGQA_DEBUG: a kernel caught (and skipped) a write
+                               outside its buffer, or recorded a TMA tile origin outside its tensor */
 } gqa_status_t;
 
 typedef enum { GQA_DTYPE_BF16 = 0, GQA_DTYPE_FP32 = 1, GQA_DTYPE_FP16 = 2 } gqa_dtype_t;
@@ -236,6 +238,7 @@ gqa_status_t gqa_decode_combine(const float* o_part, const float* lse_part, int 
  * Reads (and, if `clear` is nonzero, resets) the device error word the
  * kernels set on the current device: GQA_ERR_TIMEOUT if a bounded wait ran
  * out (the kernel then returned early and its outputs are invalid),
+ * GQA_ERR_BOUNDS (debug builds only) if a bounds check fired,
  * GQA_ERR_BAD_SEQLEN if a length was clamped, GQA_OK otherwise.  Synchronises
  * with the device (call it after the work of interest has finished).
  * After GQA_ERR_TIMEOUT from a decode kernel, treat the CUDA context as

@@ -24,7 +24,7 @@ def test_exports_every_header_function(L):
 
 
 def test_status_strings(L):
-    for code in range(7):
+    for code in range(8):
         assert g.gqa_status_string(code) not in ("", "unknown status")
     assert g.gqa_status_string(99) == "unknown status"
 
