@@ -1364,17 +1364,23 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (aborted) break;
 
       // ---------------------------------------------------------- epilogue
+      // The denominators are final once the last P is out: reduce and
+      // exchange them while the item's last value MMA still runs, and wait
+      // for it only before reading O.
       const uint32_t gl = g - 1;
       if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_E0, gl);
-      if (!local_abort)
-        local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag, p.timeout_ns);
-      local_abort = __any_sync(0xffffffffu, local_abort);
       const float lsum = detail::transpose_reduce<NC, false>(l, lane);
       const bool st_ok = wait_staging();  // staging buffer free after f3
       const uint32_t f3 = exchange((local_abort || !st_ok) ? 2u : 0u, true, lsum);
       if (f3 & 2u) { aborted = true; break; }
       float lt[NC];
       xcombine(lt, false);
+      if (!local_abort && !ptx::mbar_wait_bounded(BAR(P_EMPTY + (gl & 1u)), (gl >> 1) & 1u, abort_flag,
+                                                  p.timeout_ns)) {
+        // recorded; the warps still meet at the barriers below (outputs invalid)
+        local_abort = true;
+        detail::set_error(p.err_word, kErrTimeout, abort_flag);
+      }
 
       ptx::tc_fence_after();
       // 2 for head_dim 64 (stacked position halves, added below) and 256
