@@ -66,9 +66,13 @@ enum : unsigned { kErrTimeout = 1u, kErrBadSeqlen = 2u, kErrBounds = 4u };
 // gqa_trace_attach() (DecodeParams::trace_buf).  Compiled out otherwise.
 enum TraceEvent : int {
   TR_START = 0, TR_SETUP = 1,
-  TR_PROD_WAIT = 2, TR_PROD_K = 3, TR_PROD_V = 4, TR_PROD_PLAN = 5, TR_PROD_Q = 6,
-  TR_MMA_K = 8, TR_MMA_QK = 9, TR_MMA_P = 10, TR_MMA_V = 11, TR_MMA_PV = 12,
+  TR_PROD_WAIT = 2, TR_PROD_K = 3, TR_PROD_V = 4, TR_PROD_PLAN = 5, TR_PROD_Q = 6, TR_LENS = 7,
+  TR_MMA_K = 8, TR_MMA_QK = 9, TR_MMA_P = 10, TR_MMA_V = 11, TR_MMA_PV = 12, TR_ITER = 13, TR_PROD_T0 = 14,
+  TR_EP_CW = 15,
   TR_SM_S = 16, TR_SM_LD = 17, TR_SM_X = 18, TR_SM_PE = 19, TR_SM_PF = 20, TR_SM_E0 = 21, TR_SM_E1 = 22,
+  // epilogue of item k (one softmax thread of warpgroup 0 that holds an output row)
+  TR_EP_L = 23, TR_EP_PV = 24, TR_EP_O = 25, TR_EP_SENT = 26, TR_EP_FULL = 27, TR_EP_MERGED = 28,
+  TR_EP_EXIT = 29,
   TR_END = 31, TR_EVENTS = 32
 };
 constexpr int kTraceBlocks = 64;
@@ -367,12 +371,14 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   const bool lens_in_smem = B <= kMaxSmemB;
 
   // ---------------------------------------------------------------- set-up
-  // Right after the grid dependency the producer warp stages the clamped
-  // lengths and their unit prefix sums (PRE_READY), finds its first item and
-  // starts streaming, walking the plan's iterator itself.  Meanwhile warp 2
-  // expands the same plan into the shared item list the other roles read
-  // (PLAN_READY), and the rest allocate TMEM and zero the padding of the MMA
-  // operand buffers.
+  // Right after the grid dependency the producer warp finds its first item
+  // and starts streaming, walking the plan's iterator itself: with the
+  // balanced plan after staging the clamped lengths and their unit prefix
+  // sums (PRE_READY), which that plan's items need; with split items straight
+  // from its sequence's length in global memory, while warp 2 stages the
+  // lengths.  Warp 2 expands the same plan into the shared item list the
+  // other roles read (PLAN_READY), and the rest allocate TMEM and zero the
+  // padding of the MMA operand buffers.
   const int PLAN_READY = DRAIN + 2, OUT_FULL = DRAIN + 3, OUT_EMPTY = DRAIN + 5, PRE_READY = DRAIN + 7;
   // in-cluster merge, per softmax warpgroup and staging buffer: the k CTAs'
   // pieces of this CTA's columns have landed here (PEER_FULL, transaction
@@ -431,6 +437,39 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   // the shared list by the 32 lanes of one warp.  Owned items form a
   // contiguous run of candidates (pairs from the first one at or after this
   // CTA's first unit; split items c, c + C, ...).
+  // Clamped lengths (flagging raw lengths outside [0, S_max]) and, for the
+  // balanced plan, the exclusive prefix sums of their pairs' units, staged by
+  // the 32 lanes of one warp.
+  auto stage_lengths = [&](int lane) {
+    if (lens_in_smem) {
+      for (int i = lane; i < B; i += 32) {
+        const int raw = p.seqlens[i];
+        const int L = clamp_len(raw, plan.max_seqlen);
+        if (raw != L) detail::set_error(p.err_word, kErrBadSeqlen, nullptr);
+        s_len[i] = L;
+      }
+      __syncwarp();
+      if (plan.mode == PLAN_BALANCED) {
+        int run = 0;
+        for (int base = 0; base < B; base += 32) {
+          const int i = base + lane;
+          const int nb = i < B ? pair_units(num_blocks(s_len[i]), plan.item_units) : 0;
+          int incl = nb;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          if (i < B) s_pre[i] = run + incl - nb;
+          run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_pre[B] = run;
+      }
+    }
+    __threadfence_block();
+    __syncwarp();
+  };
+
   auto build_list = [&](int lane) {
     WorkIter base_it;
     base_it.init_warp(plan, lens_in_smem ? s_len : p.seqlens, s_len, s_pre, blockIdx.x, lane);
@@ -483,34 +522,16 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     // Inputs may be produced by the previous kernel in the stream.
     ptx::griddep_wait();
     if (lane == 0) GQA_TRACE_EVENT(TR_START, 0);
-    if (lens_in_smem) {
-      // clamped lengths and the exclusive prefix sums of their pairs' units
-      for (int i = lane; i < B; i += 32) {
-        const int raw = p.seqlens[i];
-        const int L = clamp_len(raw, plan.max_seqlen);
-        if (raw != L) detail::set_error(p.err_word, kErrBadSeqlen, nullptr);
-        s_len[i] = L;
-      }
-      __syncwarp();
-      int run = 0;
-      for (int base = 0; base < B; base += 32) {
-        const int i = base + lane;
-        const int nb = i < B ? pair_units(num_blocks(s_len[i]), plan.item_units) : 0;
-        int incl = nb;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        if (i < B) s_pre[i] = run + incl - nb;
-        run += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) s_pre[B] = run;
+    if (plan.mode == PLAN_BALANCED) {
+      stage_lengths(lane);
+      if (lane == 0) GQA_TRACE_EVENT(TR_LENS, 0);
+      if (lane == 0) ptx::mbar_arrive(BAR(PRE_READY));  // lengths and prefix sums staged
+      prod_it.init_warp(plan, lens_in_smem ? s_len : p.seqlens, s_len, s_pre, blockIdx.x, lane);
+    } else {
+      // split items: each reads its raw length (clamped the same way)
+      prod_it.init_warp(plan, p.seqlens, s_len, s_pre, blockIdx.x, lane);
     }
-    __threadfence_block();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(BAR(PRE_READY));  // lengths and prefix sums staged
-    prod_it.init_warp(plan, lens_in_smem ? s_len : p.seqlens, s_len, s_pre, blockIdx.x, lane);
+    if (lane == 0) GQA_TRACE_EVENT(TR_ITER, 0);
   } else {
     if (NPAD == 16 && threadIdx.x == kSoftmaxThread0) {
       // This CTA's first tiles are prefetched into L2 before the grid
@@ -586,7 +607,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     // Outputs and workspace may still be read by the previous kernel.
     ptx::griddep_wait();
     if (warp == 2) {
-      if (ptx::mbar_wait_bounded(BAR(PRE_READY), 0, abort_flag, p.timeout_ns)) {
+      bool staged = true;
+      if (plan.mode == PLAN_BALANCED) staged = ptx::mbar_wait_bounded(BAR(PRE_READY), 0, abort_flag, p.timeout_ns);
+      else stage_lengths(lane);
+      if (staged) {
         build_list(lane);
       } else {
         detail::set_error(p.err_word, kErrTimeout, abort_flag);
@@ -664,6 +688,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     // the plan never arrived: nothing was issued, go straight to teardown
   } else if (warp == 0) {
     if (lane == 0) {
+      GQA_TRACE_EVENT(TR_PROD_T0, 0);
       const uint64_t policy = ptx::l2_policy_evict_first();
       uint32_t tk = 0, tv = 0;  // K / V tiles issued into their rings
       int kq = 0;       // non-empty items
@@ -1007,6 +1032,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         ptx::mbar_arrive_expect_tx(full_bar, kc * static_cast<uint32_t>(dk * NC * 4 + NC * 4));
       if (!ptx::mbar_wait_cluster_bounded(full_bar, (k_out / NB) & 1u, abort_flag, p.timeout_ns))
         detail::set_error(p.err_word, kErrTimeout, abort_flag);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_FULL, k_out);
       if (!last_item && threadIdx.x == sm0) ptx::bulk_wait_read_all();  // earlier copies have read fin
       if (!last_item) ptx::named_barrier_sync(xbar, 128);                 // ... before fin is rewritten
 
@@ -1017,17 +1043,27 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       const float* recv_lse = lse_of(ob);                                // [piece][row]
       uint8_t* fin_w = fin_buf + wg * (NC * HEAD_DIM * 2);
       float* fin_lse = reinterpret_cast<float*>(fin_buf + NPAD * HEAD_DIM * 2);
-      // one (row, 4-column group) per thread and pass: NC rows x d / (4k) groups
-      for (int tw = static_cast<int>(threadIdx.x) - sm0; tw < NC * ncv; tw += 128) {
+      // One (row, 4-column group) per thread and pass: NC rows x d / (4k)
+      // groups, at most HEAD_DIM of them (k >= 2).  All passes are merged
+      // into registers first; the received pieces are then released to
+      // their senders (PEER_EMPTY) before any output is written, so that the
+      // release at cluster scope does not wait for this warp's global stores.
+      constexpr int kPasses = (Cfg::kNC * HEAD_DIM / 8 + 127) / 128;
+      float4 res[kPasses];
+      float res_lse[kPasses];
+#pragma unroll
+      for (int ps = 0; ps < kPasses; ++ps) {
+        res[ps] = make_float4(0.f, 0.f, 0.f, 0.f);
+        res_lse[ps] = -INFINITY;
+        const int tw = static_cast<int>(threadIdx.x) - sm0 + 128 * ps;
         const int n = c0 + tw / ncv, cg = tw - (tw / ncv) * ncv;
-        if (n >= nv) continue;
+        if (tw >= NC * ncv || n >= nv) continue;
         float M = -INFINITY;
 #pragma unroll
         for (int s2 = 0; s2 < kMaxClusterK; ++s2)
           if (s2 < static_cast<int>(kc)) M = fmaxf(M, recv_lse[s2 * NPAD + n]);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lse_out = -INFINITY;
         if (M != -INFINITY) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
           float W = 0.f;
 #pragma unroll
           for (int s2 = 0; s2 < kMaxClusterK; ++s2) {
@@ -1043,8 +1079,20 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           }
           const float inv = 1.0f / W;
           acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-          lse_out = M + 0.69314718055994531f * __log2f(W);
+          res[ps] = acc;
+          res_lse[ps] = M + 0.69314718055994531f * __log2f(W);
         }
+      }
+      __syncwarp();  // this warp's reads of the received pieces are done
+      if (lane == 0)
+        for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(empty_bar, s2));
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_MERGED, k_out);
+#pragma unroll
+      for (int ps = 0; ps < kPasses; ++ps) {
+        const int tw = static_cast<int>(threadIdx.x) - sm0 + 128 * ps;
+        const int n = c0 + tw / ncv, cg = tw - (tw / ncv) * ncv;
+        if (tw >= NC * ncv || n >= nv) continue;
+        const float4 acc = res[ps];
         const int col = static_cast<int>(crank) * dk + cg * 4;
         const int t = n / p.G;
         const long long grow =
@@ -1071,17 +1119,14 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           }
           if (crank == 0 && cg == 0 && p.lse != nullptr &&
               detail::write_ok(p.err_word, p.lse, p.lse_bytes, p.lse + grow, 4u))
-            p.lse[grow] = lse_out;
+            p.lse[grow] = res_lse[ps];
         } else {
           const int e = (n - c0) * dk + cg * 4;  // element of this warpgroup's merged rows
           if (out16) *reinterpret_cast<uint2*>(fin_w + e * 2) = packed;
           else *reinterpret_cast<float4*>(fin_w + e * 4) = acc;
-          if (crank == 0 && cg == 0) fin_lse[n] = lse_out;
+          if (crank == 0 && cg == 0) fin_lse[n] = res_lse[ps];
         }
       }
-      __syncwarp();  // this warp's reads of the received pieces are done
-      if (lane == 0)
-        for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(empty_bar, s2));
       if (!last_item) {
         // Later items still stream K/V tiles into this SM, and plain stores
         // would queue behind them: the merged rows leave by bulk copies.
@@ -1372,6 +1417,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       const float lsum = detail::transpose_reduce<NC, false>(l, lane);
       const bool st_ok = wait_staging();  // staging buffer free after f3
       const uint32_t f3 = exchange((local_abort || !st_ok) ? 2u : 0u, true, lsum);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_L, k_out);
       if (f3 & 2u) { aborted = true; break; }
       float lt[NC];
       xcombine(lt, false);
@@ -1381,6 +1427,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         local_abort = true;
         detail::set_error(p.err_word, kErrTimeout, abort_flag);
       }
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_PV, k_out);
 
       ptx::tc_fence_after();
       // 2 for head_dim 64 (stacked position halves, added below) and 256
@@ -1419,12 +1466,14 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         writer = r < 64;
       }
       constexpr int kRowsOut = HEAD_DIM == 256 ? 2 : 1;  // O rows of this thread: r (+ 128)
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_O, k_out);
       if constexpr (cluster_merge) {
         // the piece's rows go to the CTAs owning their columns
         if (!cluster_waited) {  // every CTA's barriers are initialised
           ptx::cluster_wait();
           cluster_waited = true;
         }
+        if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_CW, k_out);
         if (writer) {
           float inv[NC];
 #pragma unroll
@@ -1478,6 +1527,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
               lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
         }
       }
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_SENT, k_out);
       if (!hand_over(it, !iter.has_next())) { aborted = true; break; }
     }
     if constexpr (!kPvStores) {
@@ -1492,6 +1542,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       ptx::bulk_wait_all();  // this warpgroup's merged outputs are in global memory
     }
     if (aborted || local_abort) detail::set_error(p.err_word, kErrTimeout, abort_flag);
+    if (threadIdx.x == sm0) GQA_TRACE_EVENT(TR_EP_EXIT, static_cast<uint32_t>(wg));
     ptx::griddep_launch_dependents();
   }
 
