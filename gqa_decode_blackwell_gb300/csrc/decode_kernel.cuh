@@ -68,14 +68,16 @@ enum TraceEvent : int {
   TR_START = 0, TR_SETUP = 1,
   TR_PROD_WAIT = 2, TR_PROD_K = 3, TR_PROD_V = 4, TR_PROD_PLAN = 5, TR_PROD_Q = 6, TR_LENS = 7,
   TR_MMA_K = 8, TR_MMA_QK = 9, TR_MMA_P = 10, TR_MMA_V = 11, TR_MMA_PV = 12, TR_ITER = 13, TR_PROD_T0 = 14,
-  TR_EP_CW = 15,
   TR_SM_S = 16, TR_SM_LD = 17, TR_SM_X = 18, TR_SM_PE = 19, TR_SM_PF = 20, TR_SM_E0 = 21, TR_SM_E1 = 22,
-  // epilogue of item k (one softmax thread of warpgroup 0 that holds an output row)
-  TR_EP_L = 23, TR_EP_PV = 24, TR_EP_O = 25, TR_EP_SENT = 26, TR_EP_FULL = 27, TR_EP_MERGED = 28,
-  TR_EP_EXIT = 29,
+  // epilogue of the last item (one softmax thread of warpgroup 0 that holds
+  // an output row), in this order from TR_EP_L
+  TR_EP_L = 23, TR_EP_PV = 24, TR_EP_O = 25, TR_EP_CW = 26, TR_EP_SENT = 27, TR_EP_FULL = 28,
+  TR_EP_MERGED = 29, TR_EP_EXIT = 30,
   TR_END = 31, TR_EVENTS = 32
 };
 constexpr int kTraceBlocks = 64;
+constexpr int kTraceEpStamps = TR_EP_EXIT - TR_EP_L + 2;  // + the merge's compute, written as event 15
+constexpr int kTraceEpComputed = kTraceEpStamps - 1;
 #ifdef GQA_TRACE
 __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uint32_t idx) {
   if (buf == nullptr) return;
@@ -88,10 +90,19 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 #define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event(gqa_trace_buf_, (ev), (idx))
 #define GQA_TRACE_VALUE(ev, idx, v) \
   do { if (gqa_trace_buf_ != nullptr) gqa_trace_buf_[(static_cast<size_t>(blockIdx.x) * ::gqa::TR_EVENTS + (ev)) * ::gqa::kTraceBlocks + (idx)] = (v); } while (0)
+// Stamps kept in registers and written at the end (GQA_TRACE_FLUSH): a
+// global store of a stamp would otherwise hold up a later release fence.
+#define GQA_TRACE_STAMPS(arr, n) unsigned long long arr[n] = {}
+#define GQA_TRACE_STAMP(arr, i) ((arr)[i] = clock64())
+#define GQA_TRACE_FLUSH(arr, n, ev0) \
+  do { for (int i_ = 0; i_ < (n); ++i_) GQA_TRACE_VALUE(i_ + 1 < (n) ? (ev0) + i_ : 15, 0, (arr)[i_]); } while (0)
 #else
 #define GQA_TRACE_SETUP() ((void)0)
 #define GQA_TRACE_EVENT(ev, idx) ((void)(idx))  // index evaluated in both builds
 #define GQA_TRACE_VALUE(ev, idx, v) ((void)0)
+#define GQA_TRACE_STAMPS(arr, n) ((void)0)
+#define GQA_TRACE_STAMP(arr, i) ((void)0)
+#define GQA_TRACE_FLUSH(arr, n, ev0) ((void)0)
 #endif
 
 // output element types (the values of gqa_dtype_t)
@@ -328,6 +339,8 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int NWG = Cfg::kWGs;  // softmax warpgroups
   constexpr int NC = Cfg::kNC;    // columns per softmax warpgroup
   constexpr int CW = NC < 16 ? NC : 16;  // columns per TMEM load
+  constexpr int kLogD = HEAD_DIM == 64 ? 6 : (HEAD_DIM == 128 ? 7 : 8);
+  static_assert((1 << kLogD) == HEAD_DIM, "head_dim 64, 128 or 256");
   GQA_TRACE_SETUP();
 
   extern __shared__ uint8_t smem_raw[];
@@ -924,6 +937,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     float* xvals = xvals_of(wg);
     bool local_abort = false;
     uint32_t xc = 0;                  // exchange counter
+    GQA_TRACE_STAMPS(ep_ts, kTraceEpStamps);
 
     // Exchange: every warp posts flags (lane 0) and, optionally, per-column
     // values (lane l posts column transpose_col(l)); after the barrier all
@@ -1001,11 +1015,12 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       // vals: this thread's NC values of O row dr (columns c0 .. c0 + NC)
       const uint32_t kc = static_cast<uint32_t>(p.cluster_k);
       const uint32_t crank = ptx::cluster_ctarank();
-      const int dk = HEAD_DIM / static_cast<int>(kc);
+      const int ldk = kLogD - (__ffs(static_cast<int>(kc)) - 1);  // k is a power of two
+      const int dk = 1 << ldk;
       const int ob = static_cast<int>(k_out % NB);
       const uint32_t full_bar = BAR(PEER_FULL + 2 * wg + ob);
-      const uint32_t j = static_cast<uint32_t>(dr / dk);
-      const int c = dr - static_cast<int>(j) * dk;
+      const uint32_t j = static_cast<uint32_t>(dr >> ldk);
+      const int c = dr & (dk - 1);
       const uint32_t dst = ptx::map_shared_rank(
           ptx::smem_u32(obuf_of(ob)) + static_cast<uint32_t>(((static_cast<int>(crank) * dk + c) * NPAD + c0) * 4), j);
       const uint32_t rbar = ptx::map_shared_rank(full_bar, j);
@@ -1026,18 +1041,20 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       const int ob = static_cast<int>(k_out % NB);
       const uint32_t full_bar = BAR(PEER_FULL + 2 * wg + ob);
       const uint32_t empty_bar = BAR(PEER_EMPTY + 2 * wg + ob);
-      const int dk = HEAD_DIM / static_cast<int>(kc);  // output columns of this CTA
+      const int ldk = kLogD - (__ffs(static_cast<int>(kc)) - 1);  // k is a power of two
+      const int dk = 1 << ldk;  // output columns of this CTA
       // bytes every CTA sends this warpgroup: its rows of these columns and their LSEs
       if (threadIdx.x == sm0)
         ptx::mbar_arrive_expect_tx(full_bar, kc * static_cast<uint32_t>(dk * NC * 4 + NC * 4));
       if (!ptx::mbar_wait_cluster_bounded(full_bar, (k_out / NB) & 1u, abort_flag, p.timeout_ns))
         detail::set_error(p.err_word, kErrTimeout, abort_flag);
-      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_FULL, k_out);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_FULL - TR_EP_L);
       if (!last_item && threadIdx.x == sm0) ptx::bulk_wait_read_all();  // earlier copies have read fin
       if (!last_item) ptx::named_barrier_sync(xbar, 128);                 // ... before fin is rewritten
 
       constexpr float kLog2e = 1.4426950408889634f;
       const int ncv = dk >> 2;  // 4-column groups per row
+      const int lncv = ldk - 2;
       const bool out16 = p.out_dtype != kOutF32;
       const float* recv = reinterpret_cast<const float*>(obuf_of(ob));  // [piece][column][row]
       const float* recv_lse = lse_of(ob);                                // [piece][row]
@@ -1056,7 +1073,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         res[ps] = make_float4(0.f, 0.f, 0.f, 0.f);
         res_lse[ps] = -INFINITY;
         const int tw = static_cast<int>(threadIdx.x) - sm0 + 128 * ps;
-        const int n = c0 + tw / ncv, cg = tw - (tw / ncv) * ncv;
+        const int n = c0 + (tw >> lncv), cg = tw & (ncv - 1);
         if (tw >= NC * ncv || n >= nv) continue;
         float M = -INFINITY;
 #pragma unroll
@@ -1083,14 +1100,18 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           res_lse[ps] = M + 0.69314718055994531f * __log2f(W);
         }
       }
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, kTraceEpComputed);
       __syncwarp();  // this warp's reads of the received pieces are done
-      if (lane == 0)
+      // After the last item nothing is sent again: instead of these
+      // arrivals, the cluster barrier at the end keeps every CTA resident
+      // until all have merged.
+      if (!last_item && lane == 0)
         for (uint32_t s2 = 0; s2 < kc; ++s2) ptx::mbar_arrive_cluster(ptx::map_shared_rank(empty_bar, s2));
-      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_MERGED, k_out);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_MERGED - TR_EP_L);
 #pragma unroll
       for (int ps = 0; ps < kPasses; ++ps) {
         const int tw = static_cast<int>(threadIdx.x) - sm0 + 128 * ps;
-        const int n = c0 + tw / ncv, cg = tw - (tw / ncv) * ncv;
+        const int n = c0 + (tw >> lncv), cg = tw & (ncv - 1);
         if (tw >= NC * ncv || n >= nv) continue;
         const float4 acc = res[ps];
         const int col = static_cast<int>(crank) * dk + cg * 4;
@@ -1417,7 +1438,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       const float lsum = detail::transpose_reduce<NC, false>(l, lane);
       const bool st_ok = wait_staging();  // staging buffer free after f3
       const uint32_t f3 = exchange((local_abort || !st_ok) ? 2u : 0u, true, lsum);
-      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_L, k_out);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_L - TR_EP_L);
       if (f3 & 2u) { aborted = true; break; }
       float lt[NC];
       xcombine(lt, false);
@@ -1427,7 +1448,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         local_abort = true;
         detail::set_error(p.err_word, kErrTimeout, abort_flag);
       }
-      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_PV, k_out);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_PV - TR_EP_L);
 
       ptx::tc_fence_after();
       // 2 for head_dim 64 (stacked position halves, added below) and 256
@@ -1466,14 +1487,14 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         writer = r < 64;
       }
       constexpr int kRowsOut = HEAD_DIM == 256 ? 2 : 1;  // O rows of this thread: r (+ 128)
-      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_O, k_out);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_O - TR_EP_L);
       if constexpr (cluster_merge) {
         // the piece's rows go to the CTAs owning their columns
         if (!cluster_waited) {  // every CTA's barriers are initialised
           ptx::cluster_wait();
           cluster_waited = true;
         }
-        if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_CW, k_out);
+        if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_CW - TR_EP_L);
         if (writer) {
           float inv[NC];
 #pragma unroll
@@ -1527,7 +1548,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
               lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
         }
       }
-      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_EVENT(TR_EP_SENT, k_out);
+      if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_SENT - TR_EP_L);
       if (!hand_over(it, !iter.has_next())) { aborted = true; break; }
     }
     if constexpr (!kPvStores) {
@@ -1535,19 +1556,30 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     }
     if (cluster_merge && threadIdx.x == sm0) {
       // Every CTA this one sent pieces to has merged them (so the stores have
-      // landed) once it arrives on PEER_EMPTY: wait before exiting (bounded).
-      for (uint32_t i = k_out >= NB ? k_out - NB : 0u; i < k_out; ++i)
+      // landed) once it arrives on PEER_EMPTY: wait before exiting (bounded)
+      // for every item but the last, whose merge the cluster barrier at the
+      // end covers.
+      for (uint32_t i = k_out >= NB ? k_out - NB : 0u; i + 1 < k_out; ++i)
         ptx::mbar_wait_cluster_bounded(BAR(PEER_EMPTY + 2 * wg + static_cast<int>(i % NB)), (i / NB) & 1u,
                                        abort_flag, p.timeout_ns);
       ptx::bulk_wait_all();  // this warpgroup's merged outputs are in global memory
     }
     if (aborted || local_abort) detail::set_error(p.err_word, kErrTimeout, abort_flag);
-    if (threadIdx.x == sm0) GQA_TRACE_EVENT(TR_EP_EXIT, static_cast<uint32_t>(wg));
+    if (threadIdx.x == kSoftmaxThread0 + 32) {
+      GQA_TRACE_STAMP(ep_ts, TR_EP_EXIT - TR_EP_L);
+      GQA_TRACE_FLUSH(ep_ts, kTraceEpStamps, TR_EP_L);
+    }
     ptx::griddep_launch_dependents();
   }
 
   // ---------------------------------------------------------------- teardown
   if (!cluster_waited) ptx::cluster_wait();
+  if (cluster_merge) {
+    // No CTA leaves while another may still send into it or merge what it
+    // sent: every thread of the cluster has finished its role here.
+    ptx::cluster_arrive_relaxed();
+    ptx::cluster_wait();
+  }
 #ifdef GQA_TRACE
   if (lane == 0) atomicAdd(&trace_warps_done, 1u);
 #endif
