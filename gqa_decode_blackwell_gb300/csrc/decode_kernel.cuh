@@ -90,9 +90,9 @@ __device__ __forceinline__ void trace_event(unsigned long long* buf, int ev, uin
 #define GQA_TRACE_EVENT(ev, idx) ::gqa::trace_event(gqa_trace_buf_, (ev), (idx))
 #define GQA_TRACE_VALUE(ev, idx, v) \
   do { if (gqa_trace_buf_ != nullptr) gqa_trace_buf_[(static_cast<size_t>(blockIdx.x) * ::gqa::TR_EVENTS + (ev)) * ::gqa::kTraceBlocks + (idx)] = (v); } while (0)
-// Stamps kept in registers and written at the end (GQA_TRACE_FLUSH): a
+// Stamps kept in shared memory and written at the end (GQA_TRACE_FLUSH): a
 // global store of a stamp would otherwise hold up a later release fence.
-#define GQA_TRACE_STAMPS(arr, n) unsigned long long arr[n] = {}
+#define GQA_TRACE_STAMPS(arr, n) __shared__ unsigned long long arr[n]
 #define GQA_TRACE_STAMP(arr, i) ((arr)[i] = clock64())
 #define GQA_TRACE_FLUSH(arr, n, ev0) \
   do { for (int i_ = 0; i_ < (n); ++i_) GQA_TRACE_VALUE(i_ + 1 < (n) ? (ev0) + i_ : 15, 0, (arr)[i_]); } while (0)
@@ -218,43 +218,20 @@ struct DecodeCfg {
 
 namespace detail {
 
-// Reduces NP per-lane values across the 32 lanes of a warp, column by column.
-// Afterwards lane l holds the reduction of column transpose_col<NP>(l).
-template <int NP, bool IS_MAX>
-__device__ __forceinline__ float transpose_reduce(const float (&v)[NP], int lane) {
-  float a[NP];
+// Softmax thread layout: with 16x256b TMEM loads, lane i of a warp holds
+// the scores of positions i / 4 + 8 j (j = 0..3) of the warp's 32 TMEM lanes
+// for two columns, 2 (i % 4) and 2 (i % 4) + 1 of its warpgroup's eight.
+// Reduces a and b over the 8 lanes that hold the same two columns; every
+// one of them ends with the result.
+template <bool IS_MAX>
+__device__ __forceinline__ void quad_reduce(float& a, float& b) {
 #pragma unroll
-  for (int i = 0; i < NP; ++i) a[i] = v[i];
-  int off = 16;
-#pragma unroll
-  for (int w = NP / 2; w >= 1; w /= 2) {
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int j = 0; j < w; ++j) {
-      const float mine = upper ? a[w + j] : a[j];
-      const float other = upper ? a[j] : a[w + j];
-      const float recv = __shfl_xor_sync(0xffffffffu, other, off);
-      a[j] = IS_MAX ? fmaxf(mine, recv) : mine + recv;
-    }
-    off >>= 1;
+  for (int off = 4; off < 32; off <<= 1) {
+    const float ra = __shfl_xor_sync(0xffffffffu, a, off);
+    const float rb = __shfl_xor_sync(0xffffffffu, b, off);
+    a = IS_MAX ? fmaxf(a, ra) : a + ra;
+    b = IS_MAX ? fmaxf(b, rb) : b + rb;
   }
-#pragma unroll
-  for (; off >= 1; off >>= 1) {
-    const float recv = __shfl_xor_sync(0xffffffffu, a[0], off);
-    a[0] = IS_MAX ? fmaxf(a[0], recv) : a[0] + recv;
-  }
-  return a[0];
-}
-
-template <int NP>
-__device__ __forceinline__ int transpose_col(int lane) {
-  int col = 0, off = 16;
-#pragma unroll
-  for (int w = NP / 2; w >= 1; w /= 2) {
-    if (lane & off) col += w;
-    off >>= 1;
-  }
-  return col;
 }
 
 __device__ __forceinline__ void set_error(unsigned int* word, unsigned bits, volatile int* abort_flag) {
@@ -339,6 +316,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int NWG = Cfg::kWGs;  // softmax warpgroups
   constexpr int NC = Cfg::kNC;    // columns per softmax warpgroup
   constexpr int CW = NC < 16 ? NC : 16;  // columns per TMEM load
+  static_assert(NC == 8, "softmax lane layout: eight columns per warpgroup");
   constexpr int kLogD = HEAD_DIM == 64 ? 6 : (HEAD_DIM == 128 ? 7 : 8);
   static_assert((1 << kLogD) == HEAD_DIM, "head_dim 64, 128 or 256");
   GQA_TRACE_SETUP();
@@ -933,6 +911,15 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int c0 = wg * NC;                         // its first column
     const int sm0 = kSoftmaxThread0 + 128 * wg;     // its first thread
     const uint32_t xbar = 1u + 2u * static_cast<uint32_t>(wg);  // its named barrier
+    const int cq = c0 + 2 * (lane & 3);             // this lane's two score columns
+    // This lane's row of the transposed P store: column c0 + lane % 8,
+    // positions tq*32 + 8 (lane / 8) .. + 7 (one 16-byte chunk of the
+    // 64-position atom tq / 2, 128-byte swizzled).
+    const uint32_t p_addr0 = [&] {
+      const int n = c0 + (lane & 7);
+      const int chunk = (tq & 1) * 4 + (lane >> 3);
+      return ptx::smem_u32(pbuf) + static_cast<uint32_t>((tq >> 1) * (NPAD * 128) + n * 128 + ((chunk ^ (n & 7)) << 4));
+    }();
     uint32_t* xflags = xflags_of(wg);
     float* xvals = xvals_of(wg);
     bool local_abort = false;
@@ -940,17 +927,15 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
     GQA_TRACE_STAMPS(ep_ts, kTraceEpStamps);
 
     // Exchange: every warp posts flags (lane 0) and, optionally, per-column
-    // values (lane l posts column transpose_col(l)); after the barrier all
-    // four warps see the same data.  Returns the OR of the flags.
-    auto exchange = [&](uint32_t flags, bool with_vals, float val) -> uint32_t {
+    // values (after a quad reduction lane q < 4 posts columns 2q and
+    // 2q + 1); after the barrier all four warps see the same data.  Returns
+    // the OR of the flags.
+    auto exchange = [&](uint32_t flags, bool with_vals, float va, float vb) -> uint32_t {
       const uint32_t buf = xc & 1u;
       ++xc;
       if (lane == 0) xflags[buf * 4 + tq] = flags;
-      if (with_vals) {
-        // after a transpose-reduce, 32 / NC consecutive lanes share a column
-        const int col = detail::transpose_col<NC>(lane);
-        if ((lane & (32 / NC - 1)) == 0) xvals[(buf * 4 + tq) * NC + col] = val;
-      }
+      if (with_vals && lane < 4)
+        *reinterpret_cast<float2*>(xvals + (buf * 4 + tq) * NC + 2 * lane) = make_float2(va, vb);
       ptx::named_barrier_sync(xbar, 128);
       return xflags[buf * 4 + 0] | xflags[buf * 4 + 1] | xflags[buf * 4 + 2] | xflags[buf * 4 + 3];
     };
@@ -1216,7 +1201,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       if (it.blk_begin >= it.blk_end) {
         // empty item: final output O = 0, lse = -inf; partial lse = -inf
         const bool st_ok = wait_staging();
-        if (exchange(st_ok ? 0u : 2u, false, 0.f) & 2u) { aborted = true; break; }
+        if (exchange(st_ok ? 0u : 2u, false, 0.f, 0.f) & 2u) { aborted = true; break; }
         if constexpr (cluster_merge) {
           if (!cluster_waited) {  // every CTA's barriers are initialised
             ptx::cluster_wait();
@@ -1243,36 +1228,37 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         continue;
       }
       const int L = it.L;
-      // this warpgroup's columns c0 + n: running max (scaled, log2 units),
-      // per-lane denominator, and -max as the addend of the scaled scores
-      // (kNoMax while the max is -inf: any visible score then votes)
-      float m[NC], l[NC], nms[NC];
+      // This thread's columns cq, cq + 1 (cq = c0 + 2 (lane % 4)): per-lane
+      // denominators and -max as the addend of the scaled scores (max:
+      // scaled, log2 units; kNoMax while the max is -inf: any visible score
+      // then votes).  The warpgroup's -max of all its columns, the same in
+      // every thread, rescales O.
+      float l2[2] = {0.f, 0.f}, nms2[2] = {kNoMax, kNoMax};
+      float nms8[NC];
 #pragma unroll
-      for (int n = 0; n < NC; ++n) { m[n] = -INFINITY; l[n] = 0.f; nms[n] = kNoMax; }
+      for (int n = 0; n < NC; ++n) nms8[n] = kNoMax;
 
       for (int blk = it.blk_begin; blk < it.blk_end; ++blk, ++g) {
         const bool first = (blk == it.blk_begin);
         const uint32_t sl = g & 1u;
-        // ---- scores
-        float x[NC];
+        // ---- scores: x[2 j + i] = S^T(position pj = tq*32 + 8 j + lane/4, column cq + i)
+        float x[8];
         if (!local_abort)
           local_abort = !ptx::mbar_wait_bounded(BAR(S_FULL + sl), (g >> 1) & 1u, abort_flag, p.timeout_ns);
         local_abort = __any_sync(0xffffffffu, local_abort);
         if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_S, g);
         ptx::tc_fence_after();
         if (!local_abort) {
-          const uint32_t s_col = sl ? kSCol1 : kSCol0;
+          const uint32_t s_addr = tmem_base + lane_addr + (sl ? kSCol1 : kSCol0) + c0;
+          float lo[4], hi[4];
+          ptx::tmem_ld_16x256b_x1(s_addr, lo);                  // positions 0..15 of the quarter
+          ptx::tmem_ld_16x256b_x1(s_addr + (16u << 16), hi);    // positions 16..31
+          ptx::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < NC; c += CW) {
-            float v16[CW];
-            ptx::tmem_ld_32x32b<CW>(tmem_base + lane_addr + s_col + c0 + c, v16);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < CW; ++i) x[c + i] = v16[i];
-          }
+          for (int i = 0; i < 4; ++i) { x[i] = lo[i]; x[4 + i] = hi[i]; }
         } else {
 #pragma unroll
-          for (int n = 0; n < NC; ++n) x[n] = -INFINITY;
+          for (int k = 0; k < 8; ++k) x[k] = -INFINITY;
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -1286,88 +1272,131 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         // only feeds O columns that are never written out.
         const bool interior = (blk + 1) * kBlockN <= L - (p.causal ? p.nq - 1 : 0);
         if (!interior) {
-          const int pos = blk * kBlockN + r;
-          int n_min = 0;
-          if (p.causal) {
-            const int ahead = pos - (L - p.nq);
-            n_min = ahead > 0 ? ahead * p.G : 0;
-          }
-          const bool row_valid = pos < L;
 #pragma unroll
-          for (int n = 0; n < NC; ++n) {
-            const bool vis = row_valid && c0 + n >= n_min && c0 + n < nv;
-            x[n] = vis ? x[n] : -INFINITY;
+          for (int j = 0; j < 4; ++j) {
+            const int pos = blk * kBlockN + tq * 32 + 8 * j + (lane >> 2);
+            int n_min = 0;
+            if (p.causal) {
+              const int ahead = pos - (L - p.nq);
+              n_min = ahead > 0 ? ahead * p.G : 0;
+            }
+            const bool row_valid = pos < L;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const bool vis = row_valid && cq + i >= n_min && cq + i < nv;
+              x[2 * j + i] = vis ? x[2 * j + i] : -INFINITY;
+            }
           }
         }
         // t = scaled score - running max, in log2 units: one FFMA per score
         // feeds both the rescale vote and the exponent
-        float t[NC];
+        float t[8];
         bool need = false;
 #pragma unroll
-        for (int n = 0; n < NC; ++n) {
-          t[n] = fmaf(x[n], p.scale_log2, nms[n]);
-          need |= t[n] > kRescaleThreshold;
+        for (int k = 0; k < 8; ++k) {
+          t[k] = fmaf(x[k], p.scale_log2, nms2[k & 1]);
+          need |= t[k] > kRescaleThreshold;
         }
         // An item's first block always takes the max below (m is -inf; with
         // every score masked it leaves m = -inf and l = 0, as skipping it
         // would), so it needs no vote; the max exchange carries the abort flag.
         uint32_t fl = 1u;
         if (!first) {
-          fl = exchange((__any_sync(0xffffffffu, need) ? 1u : 0u) | (local_abort ? 2u : 0u), false, 0.f);
+          fl = exchange((__any_sync(0xffffffffu, need) ? 1u : 0u) | (local_abort ? 2u : 0u), false, 0.f, 0.f);
           if (fl & 2u) { aborted = true; break; }
         }
         if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_X, g);
 
         // ---- correction (only when some column's max moved past the threshold)
         if (fl & 1u) {
-          const float wmax = detail::transpose_reduce<NC, true>(x, lane);
+          float ma = fmaxf(fmaxf(x[0], x[2]), fmaxf(x[4], x[6]));
+          float mb = fmaxf(fmaxf(x[1], x[3]), fmaxf(x[5], x[7]));
+          detail::quad_reduce<true>(ma, mb);
           if (!first && !local_abort) {
             // O may be rescaled only after PV(g-1) has landed
             local_abort = !ptx::mbar_wait_bounded(BAR(P_EMPTY + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u,
                                                   abort_flag, p.timeout_ns);
           }
           local_abort = __any_sync(0xffffffffu, local_abort);
-          const uint32_t f2 = exchange(local_abort ? 2u : 0u, true, wmax);
+          const uint32_t f2 = exchange(local_abort ? 2u : 0u, true, ma, mb);
           if (f2 & 2u) { aborted = true; break; }
-          float alpha[NC], bmax[NC];
-          xcombine(bmax, true);  // of the unscaled scores: the scale is positive
+          // New maxima: M_n = max(m_n, scale * max of the block's column n).
+          // With 16 columns this lane's two columns go first (their
+          // exponentials wait on them) and the warpgroup's eight after, and an
+          // item's first block, with no O to rescale and no denominator yet,
+          // only records the maxima.  With 32 columns the eight go first and
+          // every block takes the same path (measured faster on GB300: the
+          // 608-thread kernel is at its register limit, and small changes move
+          // its spills).
+          float alpha[NC];
+          auto own_columns = [&]() {
+            const float* xv = xvals + ((xc - 1) & 1u) * 4 * NC + (cq - c0);
+            const float2 w0 = *reinterpret_cast<const float2*>(xv);
+            const float2 w1 = *reinterpret_cast<const float2*>(xv + NC);
+            const float2 w2 = *reinterpret_cast<const float2*>(xv + 2 * NC);
+            const float2 w3 = *reinterpret_cast<const float2*>(xv + 3 * NC);
+            const float bm[2] = {fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x)),
+                                 fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y))};
 #pragma unroll
-          for (int n = 0; n < NC; ++n) {
-            const float mn = fmaxf(m[n], bmax[n] * p.scale_log2);
-            const float ms = mn == -INFINITY ? 0.f : mn;
-            alpha[n] = ptx::ex2_approx(m[n] - ms);
-            m[n] = mn;
-            l[n] *= alpha[n];
-            nms[n] = mn == -INFINITY ? kNoMax : -mn;
-            t[n] = fmaf(x[n], p.scale_log2, nms[n]);
+            for (int i = 0; i < 2; ++i) {
+              const float mo = nms2[i] == kNoMax ? -INFINITY : -nms2[i];
+              const float mn = fmaxf(mo, bm[i] * p.scale_log2);
+              const float ms = mn == -INFINITY ? 0.f : mn;
+              if (!first) l2[i] *= ptx::ex2_approx(mo - ms);
+              nms2[i] = mn == -INFINITY ? kNoMax : -mn;
+            }
+          };
+          auto all_columns = [&]() {
+            float bmax[NC];
+            xcombine(bmax, true);  // of the unscaled scores: the scale is positive
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+              const float mo = nms8[n] == kNoMax ? -INFINITY : -nms8[n];
+              const float mn = fmaxf(mo, bmax[n] * p.scale_log2);
+              const float ms = mn == -INFINITY ? 0.f : mn;
+              alpha[n] = (NPAD == 16 && first) ? 0.f : ptx::ex2_approx(mo - ms);
+              nms8[n] = mn == -INFINITY ? kNoMax : -mn;
+            }
+          };
+          if constexpr (NPAD == 16) {
+            own_columns();
+            all_columns();
+          } else {
+            all_columns();
+            // this lane's two columns: entries 2 (lane % 4) and + 1
+            const int q = lane & 3;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              nms2[i] = q == 0 ? nms8[i] : q == 1 ? nms8[2 + i] : q == 2 ? nms8[4 + i] : nms8[6 + i];
+              l2[i] *= q == 0 ? alpha[i] : q == 1 ? alpha[2 + i] : q == 2 ? alpha[4 + i] : alpha[6 + i];
+            }
           }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) t[k] = fmaf(x[k], p.scale_log2, nms2[k & 1]);
           if (!first) {
             // this warpgroup's O columns: c0 + [0, NC), and for head_dim 64
             // the same columns of the second stacked half at +NPAD
             ptx::tc_fence_after();
 #pragma unroll
             for (int h2 = 0; h2 < Cfg::kOWidth / NPAD; ++h2) {
+              const uint32_t col = kOCol + static_cast<uint32_t>(h2 * NPAD + c0);
+              float o8[NC];
+              ptx::tmem_ld_32x32b<NC>(tmem_base + lane_addr + col, o8);
+              ptx::tmem_wait_ld();
 #pragma unroll
-              for (int c = 0; c < NC; c += CW) {
-                const uint32_t col = kOCol + static_cast<uint32_t>(h2 * NPAD + c0 + c);
-                float o16[CW];
-                ptx::tmem_ld_32x32b<CW>(tmem_base + lane_addr + col, o16);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < CW; ++i) o16[i] *= alpha[c + i];
-                ptx::tmem_st_32x32b<CW>(tmem_base + lane_addr + col, o16);
-              }
+              for (int i = 0; i < NC; ++i) o8[i] *= alpha[i];
+              ptx::tmem_st_32x32b<NC>(tmem_base + lane_addr + col, o8);
             }
             ptx::tmem_wait_st();
           }
         }
 
-        // ---- probabilities; the denominator is accumulated per lane
-        float pr[NC];
+        // ---- probabilities; the denominators are accumulated per lane
+        float pr[8];
 #pragma unroll
-        for (int n = 0; n < NC; ++n) {
-          pr[n] = ptx::ex2_approx(t[n]);
-          l[n] += pr[n];
+        for (int k = 0; k < 8; ++k) {
+          pr[k] = ptx::ex2_approx(t[k]);
+          l2[k & 1] += pr[k];
         }
         // P buffer sl is free once PV(g-2) has completed
         if (!local_abort && g >= 2)
@@ -1375,18 +1404,22 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         local_abort = __any_sync(0xffffffffu, local_abort);
         if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_PE, g);
         if (!local_abort) {
-          // P^T as the K-major B operand: row n, position r, 128-byte swizzle
-          uint8_t* pb = pbuf + sl * Cfg::kPBytes + (r >> 6) * (NPAD * 128);
-          const int chunk = (r & 63) >> 3, within = (r & 7) * 2;
+          // P^T as the K-major B operand (row n, positions contiguous, 128-byte
+          // swizzle): matrix j of the transposed store holds positions
+          // tq*32 + 8 j .. + 7 of columns c0 .. c0 + 7; this lane's register
+          // j packs its columns cq, cq + 1 at position 8 j + lane / 4.
+          uint32_t pw[4];
 #pragma unroll
-          for (int n = 0; n < NC; ++n) {
-            const int ng = c0 + n;
-            const int sw = chunk ^ (ng & 7);
-            if constexpr (IN_F16)
-              *reinterpret_cast<__half*>(pb + ng * 128 + sw * 16 + within) = __float2half_rn(pr[n]);
-            else
-              *reinterpret_cast<__nv_bfloat16*>(pb + ng * 128 + sw * 16 + within) = __float2bfloat16_rn(pr[n]);
+          for (int j = 0; j < 4; ++j) {
+            if constexpr (IN_F16) {
+              const __half2 h = __floats2half2_rn(pr[2 * j], pr[2 * j + 1]);
+              pw[j] = *reinterpret_cast<const uint32_t*>(&h);
+            } else {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(pr[2 * j], pr[2 * j + 1]);
+              pw[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
           }
+          ptx::stmatrix_x4_trans(p_addr0 + sl * static_cast<uint32_t>(Cfg::kPBytes), pw[0], pw[1], pw[2], pw[3]);
           // Tail block: V rows past the sequence end hold whatever the cache
           // holds there; zero them so that 0 * garbage cannot poison O.
           const int tail_rows = L - blk * kBlockN;
@@ -1435,9 +1468,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
       // for it only before reading O.
       const uint32_t gl = g - 1;
       if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_E0, gl);
-      const float lsum = detail::transpose_reduce<NC, false>(l, lane);
+      float la = l2[0], lb = l2[1];
+      detail::quad_reduce<false>(la, lb);
       const bool st_ok = wait_staging();  // staging buffer free after f3
-      const uint32_t f3 = exchange((local_abort || !st_ok) ? 2u : 0u, true, lsum);
+      const uint32_t f3 = exchange((local_abort || !st_ok) ? 2u : 0u, true, la, lb);
       if (threadIdx.x == kSoftmaxThread0 + 32) GQA_TRACE_STAMP(ep_ts, TR_EP_L - TR_EP_L);
       if (f3 & 2u) { aborted = true; break; }
       float lt[NC];
@@ -1502,7 +1536,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           float lse_d = -INFINITY;  // the LSE of column d_row, when this thread holds it
 #pragma unroll
           for (int n = 0; n < NC; ++n)
-            if (c0 + n == d_row && lt[n] > 0.f) lse_d = 0.69314718055994531f * (m[n] + __log2f(lt[n]));
+            if (c0 + n == d_row && lt[n] > 0.f) lse_d = 0.69314718055994531f * (__log2f(lt[n]) - nms8[n]);
 #pragma unroll
           for (int h2 = 0; h2 < kRowsOut; ++h2) {
             float vals[NC];
@@ -1543,7 +1577,7 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
           float lt_n = 0.f, m_n = 0.f;
 #pragma unroll
           for (int n = 0; n < NC; ++n)
-            if (c0 + n == d_row) { lt_n = lt[n]; m_n = m[n]; }
+            if (c0 + n == d_row) { lt_n = lt[n]; m_n = -nms8[n]; }
           lse_of(static_cast<int>(k_out % NB))[d_row] =
               lt_n > 0.f ? 0.69314718055994531f * (m_n + __log2f(lt_n)) : -INFINITY;
         }

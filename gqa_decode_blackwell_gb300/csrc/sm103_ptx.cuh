@@ -350,6 +350,31 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float (&v)[8])
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 lanes x 256 bits (8 consecutive 32-bit columns) from lane taddr.lane:
+// thread i of the warp receives v[0], v[1] = lane (taddr.lane + i / 4),
+// columns taddr.col + 2 (i % 4) and + 1, and v[2], v[3] = the same columns
+// of lane (taddr.lane + 8 + i / 4).
+__device__ __forceinline__ void tmem_ld_16x256b_x1(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Four 8x8 matrices of 16-bit elements stored transposed: register k of
+// thread i holds elements (i / 4, 2 (i % 4)) (low half) and (i / 4,
+// 2 (i % 4) + 1) (high half) of matrix k; thread i gives the shared-memory
+// address of row i % 8 of matrix i / 8, which receives column i % 8 of the
+// matrix (16 bytes, 16-byte aligned).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+               ::"r"(saddr), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // W (8 or 16) consecutive columns.
 template <int W>
 __device__ __forceinline__ void tmem_ld_32x32b(uint32_t taddr, float (&v)[W]) {
