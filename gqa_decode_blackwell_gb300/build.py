@@ -19,6 +19,10 @@ LIB = os.path.join(PKG, "libgqa_decode_sm103.so")
 # skipped if outside it, every TMA tile origin against its tensor; either
 # shows as GQA_ERR_BOUNDS from gqa_decode_get_error.  For testing only.
 DEBUG_LIB = os.path.join(PKG, "libgqa_decode_sm103_debug.so")
+# The same library with the decode kernel's clock64 event trace
+# (-DGQA_TRACE): gqa_trace_attach() names a device buffer that the following
+# launches stamp per CTA, role and block.  For measurement only.
+TRACE_LIB = os.path.join(PKG, "libgqa_decode_sm103_trace.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -80,6 +84,11 @@ def build(force: bool = False, out: str = LIB, extra_flags=(), verbose: bool = F
 def build_debug(force: bool = False) -> str:
     """The -DGQA_DEBUG build of the library (bounds-checked), beside the other."""
     return build(force=force, out=DEBUG_LIB, extra_flags=("-DGQA_DEBUG",))
+
+
+def build_trace(force: bool = False) -> str:
+    """The -DGQA_TRACE build of the library (event stamps), beside the other."""
+    return build(force=force, out=TRACE_LIB, extra_flags=("-DGQA_TRACE",))
 
 
 if __name__ == "__main__":
