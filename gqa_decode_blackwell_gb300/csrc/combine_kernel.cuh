@@ -150,13 +150,30 @@ gqa_combine_kernel(const CombineParams p) {
           for (int i = 0; i < VEC; ++i) acc[i] += ws * spec[s][i];
         }
       }
-      for (int s = kSpec; s < n; ++s) {
-        const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-        if (ws == 0.f) continue;  // empty split (or a weight that underflows): not used
-        float v[VEC];
-        detail::load_vec<VEC>(o_at(s), v);
+      // the rest kBatch at a time: a batch's loads go out together, then
+      // its partials are added in split order
+      constexpr int kBatch = 16 / VEC;
+      for (int s = kSpec; s < n; s += kBatch) {
+        float v[kBatch][VEC], wb[kBatch];
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) acc[i] += ws * v[i];
+        for (int j = 0; j < kBatch; ++j) {
+          const int sj = s + j;
+          const float ws = __shfl_sync(0xffffffffu, sj < 32 ? w0 : w1, sj & 31);
+          wb[j] = sj < n ? ws : 0.f;
+          if (wb[j] != 0.f) {  // an empty split (or a weight that underflows) is not read
+            detail::load_vec<VEC>(o_at(sj), v[j]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) v[j][i] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          if (wb[j] != 0.f) {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] += wb[j] * v[j][i];
+          }
+        }
       }
       const float inv = 1.0f / W;
 #pragma unroll
