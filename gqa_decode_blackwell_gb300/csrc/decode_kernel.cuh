@@ -14,7 +14,7 @@
 // the group (the PackGQA row order of "Flash Attention 4 - warp-role
 // choreography and the edges", section "Edge 2 - GQA").
 //
-// Warp roles (224 threads):
+// Warp roles (96 + 128 N/8 threads: 352 for N = 16, 608 for N = 32):
 //   warp 0      TMA producer: Q per item, then K/V tiles into an mbarrier ring
 //               in the order K0 K1 V0 K2 V1 ... (the page's split-local order),
 //               so the score MMA of block i+1 can run while block i's softmax
@@ -27,16 +27,18 @@
 //               the CUTLASS kernel ("Building a Faster GQA Decode Kernel for
 //               Blackwell SM100", section "Starting with the simple
 //               pipeline");
-//   warps 3..6  softmax / correction / epilogue warpgroup: thread r owns TMEM
-//               lane r = KV position r of S^T and row r of O^T.  It releases
-//               the S slot as soon as the scores are in registers, masks,
-//               votes on whether any column's max moved by more than the
-//               rescale threshold (8 in log2 units, "Flash Attention 4 -
-//               warp-role choreography and the edges", section "The
-//               correction"), and only then reduces the column max and
-//               rescales O in TMEM.  P goes to shared memory in one handoff
-//               as the K-major B operand of the PV MMA; the denominator is
-//               summed per lane in registers and reduced once per item.
+//   warps 3..   N/8 softmax / correction / epilogue warpgroups of 8 columns
+//               each.  A warp reads its 32 TMEM lanes (KV positions) of S^T
+//               with 16x256b loads: lane i holds positions i/4 + 8j of two
+//               columns.  It releases the S slot as soon as the scores are in
+//               registers, masks, votes on whether any column's max moved by
+//               more than the rescale threshold (8 in log2 units, "Flash
+//               Attention 4 - warp-role choreography and the edges", section
+//               "The correction"), and only then reduces the column max and
+//               rescales O in TMEM (thread r: row r of O^T).  P^T goes to
+//               shared memory, as the K-major B operand of the PV MMA, in one
+//               transposed stmatrix per thread; the denominators are summed
+//               per lane in registers and reduced once per item.
 //
 // head_dim 64 uses M = 128 for the PV MMA by stacking the two 64-position
 // halves of the block along M: A = [V_lo^T ; V_hi^T] (128 x 64), B =
