@@ -1,0 +1,50 @@
+"""The ncu summaries under profiles/ are tied to the decode kernel's code by a
+digest that ignores comments and layout: the committed summaries match the
+committed sources, a comment edit keeps the digest, a code edit changes it,
+and bench.py reads a summary's DRAM bytes only while they match."""
+import glob
+import os
+
+import bench
+
+
+def test_committed_summaries_match_the_kernel_sources():
+    digest = bench.kernel_source_digest()
+    paths = sorted(glob.glob(os.path.join(bench.PROFILES, "decode_kernel_*.md")))
+    assert paths
+    for path in paths:
+        workload = os.path.basename(path)[len("decode_kernel_"):-len(".md")]
+        traffic, source = bench.ncu_traffic(workload)
+        assert traffic is not None and traffic > 0, (path, source, digest)
+
+
+def test_code_only_ignores_comments_and_layout():
+    a = 'int f(int x) {  // first\n  return x + 1; /* two */ }\nconst char* s = "//kept /*kept*/";\n'
+    b = 'int f(int x) { return x + 1; }\n// another comment\nconst char* s = "//kept /*kept*/";'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert "//kept /*kept*/" in bench._code_only(a)
+    c = a.replace("x + 1", "x + 2")
+    assert bench._code_only(c) != bench._code_only(a)
+    assert bench._code_only("char q = '\"'; int y; // \" not a string") == "char q = '\"'; int y;"
+
+
+def test_summary_ignored_once_the_code_changes(tmp_path, monkeypatch):
+    src = tmp_path / "gqa_decode_blackwell_gb300" / "csrc"
+    src.mkdir(parents=True)
+    for name in bench.KERNEL_SOURCES:
+        with open(os.path.join(bench.ROOT, "gqa_decode_blackwell_gb300", "csrc", name)) as f:
+            (src / name).write_text(f.read())
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    for path in glob.glob(os.path.join(bench.PROFILES, "decode_kernel_*.md")):
+        with open(path) as f:
+            (prof / os.path.basename(path)).write_text(f.read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "PROFILES", str(prof))
+    assert bench.ncu_traffic("ragged")[0] is not None
+    k = src / "decode_kernel.cuh"
+    k.write_text(k.read_text() + "\n// a comment\n")
+    assert bench.ncu_traffic("ragged")[0] is not None
+    k.write_text(k.read_text() + "\nstatic_assert(true, \"\");\n")
+    traffic, why = bench.ncu_traffic("ragged")
+    assert traffic is None and "changed" in why
