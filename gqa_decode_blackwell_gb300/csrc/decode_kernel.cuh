@@ -1302,11 +1302,10 @@ gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
         // An item's first block always takes the max below (m is -inf; with
         // every score masked it leaves m = -inf and l = 0, as skipping it
         // would), so it needs no vote; the max exchange carries the abort flag.
+        // The vote is one named barrier that ORs the warpgroup's predicates;
+        // an abort joins it, and the max exchange below then carries it.
         uint32_t fl = 1u;
-        if (!first) {
-          fl = exchange((__any_sync(0xffffffffu, need) ? 1u : 0u) | (local_abort ? 2u : 0u), false, 0.f, 0.f);
-          if (fl & 2u) { aborted = true; break; }
-        }
+        if (!first) fl = ptx::named_barrier_or(xbar, 128, need || local_abort) ? 1u : 0u;
         if (threadIdx.x == kSoftmaxThread0) GQA_TRACE_EVENT(TR_SM_X, g);
 
         // ---- correction (only when some column's max moved past the threshold)
