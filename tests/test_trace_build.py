@@ -105,3 +105,64 @@ def test_trace_stamps_follow_the_pipeline(trace_lib, name, splits):
         ep += [a[TR_EP_EXIT, 0], a[TR_END, 0]]
         assert all(x > 0 for x in ep), (name, c, mode, ep)
         assert all(x <= y for x, y in zip(ep, ep[1:])), (name, c, mode, ep)
+
+
+# ------------------------------------------------------------------ trace tool
+def test_trace_tool_events_match_the_kernel():
+    """gqa_decode_blackwell_gb300.trace names the kernel's TraceEvent values."""
+    import os
+    import re
+
+    from gqa_decode_blackwell_gb300 import trace
+
+    src = open(os.path.join(os.path.dirname(g.__file__), "csrc", "decode_kernel.cuh")).read()
+    enum = src[src.index("enum TraceEvent"):]
+    enum = enum[:enum.index("};")]
+    pairs = dict((k, int(v)) for k, v in re.findall(r"TR_([A-Z0-9_]+)\s*=\s*(\d+)", enum))
+    pairs.pop("EVENTS")
+    assert pairs == {k: v for k, v in trace.EVENTS.items() if k != "EP_COMPUTED"}
+    assert trace.NUM_EVENTS == 32 and trace.BLOCKS == int(re.search(r"kTraceBlocks = (\d+)", src).group(1))
+    # the merge's compute stamp is flushed to the one free slot
+    assert "(ev0) + i_ : 15," in src and trace.EVENTS["EP_COMPUTED"] == 15
+
+
+def test_trace_tool_summary_of_a_synthetic_trace():
+    from gqa_decode_blackwell_gb300 import trace
+
+    E = trace.EVENTS
+    t = np.zeros((4, trace.NUM_EVENTS, trace.BLOCKS), dtype=np.int64)
+    for c, base in ((0, 1000), (1, 5000)):       # two working CTAs, six blocks each
+        a = t[c]
+        a[E["START"], 0] = base
+        a[E["PROD_PLAN"], 0] = base + 100
+        a[E["PROD_K"], 0] = base + 200
+        a[E["MMA_K"], 0] = base + 300
+        for g in range(6):
+            s = base + 1000 + 500 * g
+            a[E["MMA_QK"], g] = s - 50
+            a[E["SM_S"], g], a[E["SM_LD"], g], a[E["SM_X"], g] = s, s + 10, s + 30
+            a[E["SM_PE"], g], a[E["SM_PF"], g] = s + 60, s + 100
+        a[E["END"], 0] = base + 1000 + 500 * 5 + 100 + 777
+    summ = trace.summarize(t)
+    assert summ["ctas"] == 2
+    assert summ["start_up"]["first item"] == 100 and summ["start_up"]["first K landed"] == 300
+    assert summ["softmax_per_block"] == {"S load": 10, "vote": 20, "exponent": 30, "P store": 40, "period": 500}
+    assert summ["first_block"] == 100 and summ["last_P_full_to_end"] == 777
+
+
+@pytest.mark.gpu
+def test_trace_tool_on_the_speculative_workload():
+    from gqa_decode_blackwell_gb300 import trace
+
+    dev = torch.device("cuda:0")
+    cfg = workloads.CONFIGS["spec"]
+    inp = workloads.make_inputs(cfg).to(dev)
+    out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(inp.q.shape[:3], dtype=torch.float32, device=dev)
+    t = trace.capture(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, out, lse, 0, causal=cfg.causal)
+    summ = trace.summarize(t)
+    assert summ["ctas"] == 128  # two pieces per (batch, KV head) pair, merged in clusters of two
+    steps = summ["softmax_per_block"]
+    assert all(v is not None and v > 0 for v in steps.values()), summ
+    assert steps["period"] >= steps["S load"] + steps["vote"] + steps["exponent"] + steps["P store"], summ
+    assert summ["last_P_full_to_end"] > 0 and summ["start_up"]["first K landed"] > 0, summ
