@@ -389,20 +389,26 @@ def bench_ours(args, cfg, world, rank, local):
     if g.gqa_decode_get_error(clear=True) != g.GQA_OK:
         raise RuntimeError("decode reported a device error in the eager calls")
 
-    # end to end through the C ABI with pinned host buffers
+    # end to end through the C ABI with pinned host buffers: each step copies
+    # q, the lengths and every sequence's live key/value rows (positions
+    # [0, L_b), the ones the call reads; rows past a length are left as they
+    # are on the device), runs the call and reads out and lse back.
     e2e = None
     if not args.no_e2e:
-        h = [host.q.pin_memory(), host.k_cache.pin_memory(), host.v_cache.pin_memory(), host.seqlens.pin_memory()]
-        d = [torch.empty_like(x, device=dev) for x in h]
+        hq, hk, hv, hs = (x.pin_memory() for x in (host.q, host.k_cache, host.v_cache, host.seqlens))
+        dq, dk, dv, ds = (torch.empty_like(x, device=dev) for x in (hq, hk, hv, hs))
+        lens = host.seqlens.tolist()
+        pieces = [(dq, hq), (ds, hs)] + [(dc[b, :n], hc[b, :n]) for dc, hc in ((dk, hk), (dv, hv))
+                                         for b, n in enumerate(lens) if n > 0]
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in h)
+        h2d = sum(src.numel() * src.element_size() for _, src in pieces)
         d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
         def e2e_step():
-            for dst, src in zip(d, h):
+            for dst, src in pieces:
                 dst.copy_(src, non_blocking=True)
-            g.gqa_decode_attn(d[0], d[1], d[2], d[3], out, lse, splits, ws, causal=cfg.causal, reduction=red)
+            g.gqa_decode_attn(dq, dk, dv, ds, out, lse, splits, ws, causal=cfg.causal, reduction=red)
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -417,9 +423,20 @@ def bench_ours(args, cfg, world, rank, local):
         a1.record(cur)
         torch.cuda.synchronize()
         ms_e2e = reduce_max(a0.elapsed_time(a1) / args.e2e_steps, world, dev)
+        # the copied-in result must equal, bit for bit, a call on the
+        # device-resident inputs (the rows left uncopied are never read)
+        g.gqa_decode_attn(base.q, base.k_cache, base.v_cache, base.seqlens, out, lse, splits, ws,
+                          causal=cfg.causal, reduction=red)
+        torch.cuda.synchronize()
+        same = all(torch.equal(a.contiguous().view(torch.uint8), b.cpu().contiguous().view(torch.uint8))
+                   for a, b in ((h_out, out), (h_lse, lse)))
+        if not same or g.gqa_decode_get_error(clear=True) != g.GQA_OK:
+            raise RuntimeError("end-to-end result differs from the call on device-resident inputs")
         e2e = {"value": round(world * kv_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(ms_e2e, 4), "steps": args.e2e_steps, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+               "d2h_bytes_per_step": d2h,
+               "copies": "q, lengths and each sequence's live K/V rows from pinned host memory, one stream",
+               "checked": "bit-identical to the call on device-resident inputs"}
 
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (ms_decode * 1e-3) / 1e9
