@@ -268,6 +268,16 @@ def pages_method(steps: GraphSteps, dec_steps: GraphSteps, stream, rounds: int =
     return min(call), min(dec)
 
 
+def live_copy_pieces(dst, src, lens):
+    """(destination, source) pairs for one end-to-end step: all of q and of
+    the lengths, and rows [0, L_b) of each sequence's key and value cache
+    ([B, capacity, Hkv, d]; a sequence's live rows are one contiguous run).
+    dst and src are (q, k_cache, v_cache, seqlens) tuples of equal shapes."""
+    (dq, dk, dv, ds), (hq, hk, hv, hs) = dst, src
+    return [(dq, hq), (ds, hs)] + [(dc[b, :n], hc[b, :n]) for dc, hc in ((dk, hk), (dv, hv))
+                                   for b, n in enumerate(lens) if n > 0]
+
+
 def bench_ours(args, cfg, world, rank, local):
     import gqa_decode_blackwell_gb300 as g
     from gqa_decode_blackwell_gb300 import build as gbuild
@@ -397,9 +407,7 @@ def bench_ours(args, cfg, world, rank, local):
     if not args.no_e2e:
         hq, hk, hv, hs = (x.pin_memory() for x in (host.q, host.k_cache, host.v_cache, host.seqlens))
         dq, dk, dv, ds = (torch.empty_like(x, device=dev) for x in (hq, hk, hv, hs))
-        lens = host.seqlens.tolist()
-        pieces = [(dq, hq), (ds, hs)] + [(dc[b, :n], hc[b, :n]) for dc, hc in ((dk, hk), (dv, hv))
-                                         for b, n in enumerate(lens) if n > 0]
+        pieces = live_copy_pieces((dq, dk, dv, ds), (hq, hk, hv, hs), host.seqlens.tolist())
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         h2d = sum(src.numel() * src.element_size() for _, src in pieces)

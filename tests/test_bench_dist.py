@@ -50,3 +50,29 @@ def test_single_process_reduce_is_identity():
     import bench
 
     assert bench.reduce_max(3.25, 1) == 3.25
+
+
+def test_live_copy_pieces_cover_exactly_the_live_rows():
+    """The end-to-end step's copy list: q and the lengths whole, and rows
+    [0, L_b) of every sequence's K and V (empty sequences copy nothing).
+    Copying it onto a poisoned destination leaves exactly the rows past
+    each length poisoned."""
+    import torch
+
+    import bench
+
+    B, cap, Hkv, d, lens = 4, 37, 2, 8, [37, 0, 5, 19]
+    src = (torch.randn(B, 1, 4, d), torch.randn(B, cap, Hkv, d), torch.randn(B, cap, Hkv, d),
+           torch.tensor(lens, dtype=torch.int32))
+    dst = tuple(torch.full_like(x, -7) for x in src)
+    pieces = bench.live_copy_pieces(dst, src, lens)
+    assert len(pieces) == 2 + 2 * sum(1 for n in lens if n > 0)
+    for a, b in pieces:
+        a.copy_(b)
+    assert torch.equal(dst[0], src[0]) and torch.equal(dst[3], src[3])
+    for c in (1, 2):
+        for b, n in enumerate(lens):
+            assert torch.equal(dst[c][b, :n], src[c][b, :n])
+            assert bool((dst[c][b, n:] == -7).all())
+    moved = sum(s.numel() * s.element_size() for _, s in pieces)
+    assert moved == (src[0].numel() + 2 * sum(lens) * Hkv * d) * 4 + 4 * B
