@@ -245,6 +245,13 @@ def check_cluster(lens, Hkv, s_max, sm, k, G=4, nq=1, num_splits=0, reduction=g.
         seen[(b, h, j)] += 1
     assert set(seen) == {(b, h, j) for b in range(len(lens)) for h in range(Hkv) for j in range(k)}
     assert set(seen.values()) == {1}
+    # The merge exchanges item by item: the k CTAs of a cluster must take the
+    # same pairs in the same order (items are listed in processing order).
+    order = collections.defaultdict(list)
+    for c, b, h, *_ in items:
+        order[int(c)].append((int(b), int(h)))
+    for q in range(Q):
+        assert all(order[q * k + j] == order[q * k] for j in range(1, k))
 
 
 @pytest.mark.parametrize("B,Hkv,L,G,nq,k", [
