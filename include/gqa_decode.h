@@ -95,7 +95,7 @@ typedef struct {
   int q_tokens;    /* nq >= 1 new query tokens per sequence */
   int q_heads;     /* Hq, a multiple of kv_heads */
   int kv_heads;    /* Hkv >= 1 */
-  int head_dim;    /* d: 64 or 128 */
+  int head_dim;    /* d: 64, 128 or 256 */
   int max_seqlen;  /* S_max >= 1: cache capacity along positions */
   float scale;     /* softmax scale; 0 selects 1/sqrt(head_dim) */
   int causal;      /* nonzero: causal mask among the nq new tokens */
@@ -228,7 +228,7 @@ gqa_status_t gqa_decode_splitkv(const gqa_desc_t* desc, const void* q, const voi
  *   lse_part  fp32 [num_splits, rows]
  *   out       [rows, head_dim] of out_dtype, 16-byte aligned
  *   lse       fp32 [rows] or NULL
- * num_splits: 1..64; head_dim: 64 or 128; rows >= 0.
+ * num_splits: 1..64; head_dim: 64, 128 or 256; rows >= 0.
  */
 gqa_status_t gqa_decode_combine(const float* o_part, const float* lse_part, int num_splits,
                                 int64_t rows, int head_dim, void* out, int out_dtype, float* lse,
