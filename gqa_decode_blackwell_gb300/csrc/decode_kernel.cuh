@@ -46,6 +46,20 @@
 // half's contribution and lanes 64..127 x columns [N, 2N) the second's; the
 // cross quadrants are discarded and the epilogue adds the two halves.
 //
+// head_dim 256 streams each block as two ring tiles of 128 positions x 128
+// elements, its d-halves (K lo, K hi, V lo, V hi).  The score MMA accumulates
+// S^T over both K halves before it commits, and the value issuer runs one
+// M = 128 chain per V half into a TMEM accumulator of its own.  The epilogue
+// then writes O rows r and r + 128.
+//
+// Merging the splits (DecodeParams / plan mode): either each CTA writes fp32
+// partials and an LSE per row for the combine kernel, or (CLUSTER) the k
+// splits of a pair run as the k CTAs of one thread-block cluster.  In the
+// cluster case the CTAs exchange their normalised rows and LSEs through
+// distributed shared memory and merge them in fixed split order, with no
+// second launch ("Building a Faster GQA Decode Kernel for Blackwell SM100",
+// section "Reducing inside a thread block cluster").
+//
 // Every wait is bounded.  A wait that times out sets the device error word,
 // raises a CTA-wide abort flag and the roles leave their loops in step (the
 // softmax warps decide uniformly, at their exchange barriers), wait for their
