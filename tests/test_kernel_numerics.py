@@ -1,0 +1,82 @@
+"""The regression bounds of the GPU parity tests, derived on the CPU.
+
+tests/kernel_numerics.py repeats the decode kernel's rounding steps.  These
+tests check three things:
+- the model itself is right: without its two departures from exact
+  arithmetic (P rounded to bf16, a stale running max) it agrees with the
+  fp64 oracle to fp32 round-off, causal masking and split merging included;
+- the short-row bound REG_ABS is set by the stale max: a peaked row's worst
+  error falls when the max is kept current and stays under the bound
+  either way;
+- the workloads' rows stay well under REG_LONG and REG_LSE.
+Split pieces follow the documented partition (oracle.split_ranges) with the
+piece counts that the automatic plan takes for these shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_decode_blackwell_gb300 import workloads
+from tests import kernel_numerics as km
+from tests.tolerances import REG_ABS, REG_LONG, REG_LSE
+
+SHORT = workloads.shrink(workloads.CONFIGS["llama8b"], batch=2, seqlen=700)  # scale 0.3: peaked rows
+
+
+def _run(cfg, splits, *, scale=0.0, out16=True, threshold=8.0, round_p=True):
+    inp = workloads.make_inputs(cfg)
+    sc = scale if scale else 1.0 / float(cfg.head_dim) ** 0.5
+    ref_o, ref_l = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, scale=sc, causal=cfg.causal)
+    begin, end = oracle.split_ranges(inp.seqlens.tolist(), splits)
+
+    def ranges(b):
+        return [(int(begin[s, b]), int(end[s, b])) for s in range(splits)]
+
+    o, l = km.decode(inp.q.float().numpy(), inp.k_cache.float().numpy(), inp.v_cache.float().numpy(),
+                     inp.seqlens.numpy(), ranges, scale=sc, causal=cfg.causal, threshold=threshold,
+                     out16=out16, round_p=round_p)
+    fin = ~np.isneginf(ref_l)
+    assert np.array_equal(np.isneginf(l), ~fin)
+    diff = np.abs(o - ref_o)
+    if out16:  # beyond one bf16 ulp of the reference, as the GPU tests measure it
+        ax = np.maximum(np.abs(ref_o), 2.0 ** -126)
+        diff = diff - np.exp2(np.floor(np.log2(ax)) - 7)
+    return float(diff.max()), float(np.abs(l[fin] - ref_l[fin]).max())
+
+
+def test_bf16_rounding_is_round_to_nearest_even():
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(4096).astype(np.float32) * 300,
+                        np.float32([0.0, -0.0, 1.0, 1.00390625, 1.01171875, 3.0e-39, 65504.0, -2.5e-3])])
+    # 1 + 2^-8 and 1 + 3 * 2^-8 sit halfway between bf16 neighbours: ties to even
+    want = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(km.to_bf16(x), want)
+
+
+@pytest.mark.parametrize("name,splits", [("tiny", 1), ("spec", 2), ("short", 4), ("spec-edge", 5)])
+def test_model_without_its_roundings_matches_the_oracle(name, splits):
+    cfg = {"short": SHORT,
+           "spec-edge": workloads.shrink(workloads.CONFIGS["spec"], batch=5, seqlen=1000)}.get(
+        name, workloads.CONFIGS.get(name))
+    err_o, err_l = _run(cfg, splits, scale=0.3 if name == "short" else 0.0, out16=False, threshold=0.0,
+                        round_p=False)
+    assert err_o < 1e-5 and err_l < 1e-5  # fp32 round-off; the modelled roundings cost 1e-4 to 5e-3
+
+
+def test_stale_max_sets_the_short_row_bound():
+    """Peaked rows (scale 0.3, 700 keys, four pieces per pair, as the
+    automatic plan takes them): the error with the threshold-8 max is several
+    times the error with a current max, and both stay under REG_ABS."""
+    stale, lse_err = _run(SHORT, 4, scale=0.3, out16=False)
+    current, _ = _run(SHORT, 4, scale=0.3, out16=False, threshold=0.0)
+    stale16, _ = _run(SHORT, 4, scale=0.3, out16=True)
+    assert 2e-3 < stale < REG_ABS
+    assert current < stale / 2
+    assert stale16 < REG_ABS and lse_err < REG_LSE
+
+
+@pytest.mark.parametrize("name,splits", [("llama8b", 2), ("spec", 2), ("llama70b", 8)])
+def test_workload_rows_sit_well_under_the_long_bound(name, splits):
+    err_o, err_l = _run(workloads.CONFIGS[name], splits)
+    assert err_o < REG_LONG / 2 and err_l < REG_LSE / 4

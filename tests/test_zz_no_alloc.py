@@ -17,11 +17,10 @@ import torch
 import gqa_decode_blackwell_gb300 as g
 from gqa_decode_blackwell_gb300 import build as gbuild
 from gqa_decode_blackwell_gb300 import workloads
+from tests.tolerances import LSE_TOL, OUT_TOL
 
 pytestmark = pytest.mark.gpu
 
-OUT_TOL = 2e-2
-LSE_TOL = 1e-3
 STATIC_BYTES = 32 * 1024 * 1024
 DEV = torch.device("cuda:0")
 
