@@ -128,3 +128,21 @@ def make_inputs(cfg: DecodeConfig, seed: Optional[int] = None, capacity: Optiona
 def shrink(cfg: DecodeConfig, **changes) -> DecodeConfig:
     """A smaller variant of a config (same structure) for fast parity tests."""
     return replace(cfg, **changes)
+
+
+def head_dim_256_inputs(which: int) -> DecodeInputs:
+    """head_dim 256 test inputs, seeded randn rounded to bf16 (seed 600 +
+    which; draw order q, k, v), scale 1/16.  which = 0: the split-reduction
+    trace shape of "Building a Faster GQA Decode Kernel for Blackwell SM100"
+    (one sequence of 32768 positions, 32 query heads on one KV head); which =
+    1: a 16-column batch of lengths 9001, 3000 and 129."""
+    gen = torch.Generator().manual_seed(600 + which)
+    if which == 0:
+        B, nq, Hq, Hkv, lens = 1, 1, 32, 1, [32768]
+    else:
+        B, nq, Hq, Hkv, lens = 3, 1, 16, 2, [9001, 3000, 129]
+    s_max = max(lens)
+    q = torch.randn(B, nq, Hq, 256, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, s_max, Hkv, 256, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, s_max, Hkv, 256, generator=gen).to(torch.bfloat16)
+    return DecodeInputs(None, q, k, v, torch.tensor(lens, dtype=torch.int32), 1 / 16)

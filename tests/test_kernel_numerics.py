@@ -25,16 +25,22 @@ SHORT = workloads.shrink(workloads.CONFIGS["llama8b"], batch=2, seqlen=700)  # s
 
 
 def _run(cfg, splits, *, scale=0.0, out16=True, threshold=8.0, round_p=True):
-    inp = workloads.make_inputs(cfg)
-    sc = scale if scale else 1.0 / float(cfg.head_dim) ** 0.5
-    ref_o, ref_l = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, scale=sc, causal=cfg.causal)
+    return _compare(workloads.make_inputs(cfg), splits, scale=scale, causal=cfg.causal, out16=out16,
+                    threshold=threshold, round_p=round_p)
+
+
+def _compare(inp, splits, *, scale=0.0, causal=False, out16=True, threshold=8.0, round_p=True):
+    """Max error of the model against the oracle: |dO| (beyond one bf16 ulp
+    for 16-bit outputs) and |dlse|, with `splits` pieces per sequence."""
+    sc = scale if scale else 1.0 / float(inp.q.shape[-1]) ** 0.5
+    ref_o, ref_l = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, scale=sc, causal=causal)
     begin, end = oracle.split_ranges(inp.seqlens.tolist(), splits)
 
     def ranges(b):
         return [(int(begin[s, b]), int(end[s, b])) for s in range(splits)]
 
     o, l = km.decode(inp.q.float().numpy(), inp.k_cache.float().numpy(), inp.v_cache.float().numpy(),
-                     inp.seqlens.numpy(), ranges, scale=sc, causal=cfg.causal, threshold=threshold,
+                     inp.seqlens.numpy(), ranges, scale=sc, causal=causal, threshold=threshold,
                      out16=out16, round_p=round_p)
     fin = ~np.isneginf(ref_l)
     assert np.array_equal(np.isneginf(l), ~fin)
@@ -80,3 +86,14 @@ def test_stale_max_sets_the_short_row_bound():
 def test_workload_rows_sit_well_under_the_long_bound(name, splits):
     err_o, err_l = _run(workloads.CONFIGS[name], splits)
     assert err_o < REG_LONG / 2 and err_l < REG_LSE / 4
+
+
+@pytest.mark.parametrize("which,splits", [(0, 8), (1, 3)])
+def test_head_dim_256_rows(which, splits):
+    """The head_dim 256 parity cases, held to the long-row bound on the GPU.
+    The trace shape (32768 keys) sits far below it.  The ragged batch's
+    largest error is in its 129-key sequence, a short row whose two pieces
+    each take their max exactly: plain bf16 rounding of p, 7.8e-4, with
+    only a 1.3x margin to the bound, so the model pins that margin here."""
+    err_o, err_l = _compare(workloads.head_dim_256_inputs(which), splits, out16=False)
+    assert err_o < (REG_LONG / 4 if which == 0 else REG_LONG) and err_l < REG_LSE / 4

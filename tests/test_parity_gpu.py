@@ -460,18 +460,9 @@ _LONG_REF = {}
 # dimension 256 -- and a 16-column shape with ragged lengths.
 @functools.lru_cache(maxsize=1)
 def d256_case(which):
-    gen = torch.Generator().manual_seed(600 + which)
-    if which == 0:
-        B, nq, Hq, Hkv, lens = 1, 1, 32, 1, [32768]
-    else:
-        B, nq, Hq, Hkv, lens = 3, 1, 16, 2, [9001, 3000, 129]
-    s_max = max(lens)
-    q = torch.randn(B, nq, Hq, 256, generator=gen).to(torch.bfloat16)
-    k = torch.randn(B, s_max, Hkv, 256, generator=gen).to(torch.bfloat16)
-    v = torch.randn(B, s_max, Hkv, 256, generator=gen).to(torch.bfloat16)
-    sl = torch.tensor(lens, dtype=torch.int32)
-    ref = oracle.decode(q, k, v, sl)
-    return workloads.DecodeInputs(None, q, k, v, sl, 1 / 16).to(DEV), ref
+    inp = workloads.head_dim_256_inputs(which)
+    ref = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens)
+    return inp.to(DEV), ref
 
 
 D256 = [(0, 8, "auto"), (0, 8, "combine"), (0, 0, "auto"), (0, 1, "auto"), (0, 4, "cluster"),
