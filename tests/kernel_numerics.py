@@ -10,11 +10,11 @@ oracle does not:
   exceeds it by more than the rescale threshold (8; "Flash Attention 4 -
   warp-role choreography and the edges", section "The correction").  Every
   column of that warpgroup then takes its new max;
-- p = 2^t in fp32, summed in fp32 for the denominator but rounded to bf16 for
-  the value product;
+- p = 2^t in fp32, summed in fp32 for the denominator but rounded to the
+  input type (bf16 or fp16) for the value product;
 - each split piece normalised in fp32, its LSE in natural-log units;
 - the pieces merged with fp32 weights 2^((lse_s - M) log2 e) in split order,
-  and the output rounded to bf16 when it is 16-bit.
+  and the output rounded to its 16-bit type when it has one.
 
 The model shares nothing with the kernels and is not the oracle: parity is
 always checked against the oracle.  A column n of a (batch, KV head) pair is
@@ -36,11 +36,19 @@ def to_bf16(x):
     return u.astype(np.uint32).view(np.float32)
 
 
+def to_fp16(x):
+    """fp32 -> fp16 (round to nearest, ties to even), returned as fp32."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
+ROUND = {"bf16": to_bf16, "fp16": to_fp16, None: lambda x: np.asarray(x, dtype=np.float32)}
+
+
 def f32(x):
     return np.asarray(x, dtype=np.float64).astype(np.float32)
 
 
-def piece(qc, k, v, lo, hi, L, nq, G, scale, causal, threshold, round_p=True):
+def piece(qc, k, v, lo, hi, L, nq, G, scale, causal, threshold, p_type="bf16"):
     """One split piece, keys [lo, hi), of one (batch, KV head) pair.
     qc: [C, d] query columns (C = nq G), k, v: [positions, d].
     Returns the normalised O [C, d] and the LSE [C] (natural log), fp32."""
@@ -78,7 +86,7 @@ def piece(qc, k, v, lo, hi, L, nq, G, scale, causal, threshold, round_p=True):
         t = f32(s.astype(np.float64) * sl2 - ms)
         p = f32(np.exp2(t.astype(np.float64)))
         l = f32(l + p.sum(axis=0, dtype=np.float32))
-        pv = to_bf16(p) if round_p else p
+        pv = ROUND[p_type](p)
         O = f32(O.astype(np.float64) + pv.T.astype(np.float64) @ v[b0:b1].astype(np.float64))
     with np.errstate(divide="ignore", invalid="ignore"):
         Oo = np.where(l[:, None] > 0, f32(O / l[:, None]), np.float32(0))
@@ -87,12 +95,14 @@ def piece(qc, k, v, lo, hi, L, nq, G, scale, causal, threshold, round_p=True):
     return Oo, lse
 
 
-def decode(q, k_cache, v_cache, seqlens, ranges, *, scale, causal=False, threshold=8.0, out16=True,
-           round_p=True):
+def decode(q, k_cache, v_cache, seqlens, ranges, *, scale, causal=False, threshold=8.0, p_type="bf16",
+           out_type="bf16"):
     """q [B, nq, Hq, d], caches [B, S_max, Hkv, d] (float arrays holding the
     16-bit inputs' values), seqlens [B]; ranges(b) -> the (lo, hi) key ranges
-    of sequence b's split pieces.  Returns O [B, nq, Hq, d] and lse
-    [B, nq, Hq] as the kernel's arithmetic produces them (float64 arrays)."""
+    of sequence b's split pieces.  p_type / out_type: the type P is rounded to
+    for the value product and the output type ("bf16", "fp16"; None: fp32,
+    no rounding).  Returns O [B, nq, Hq, d] and lse [B, nq, Hq] as the
+    kernel's arithmetic produces them (float64 arrays)."""
     B, nq, Hq, d = q.shape
     Hkv = k_cache.shape[2]
     G = Hq // Hkv
@@ -105,7 +115,7 @@ def decode(q, k_cache, v_cache, seqlens, ranges, *, scale, causal=False, thresho
             Os, Ls = [], []
             for lo, hi in ranges(b):
                 o_, l_ = piece(qc, k_cache[b, :, h], v_cache[b, :, h], lo, hi, L, nq, G, scale, causal,
-                               threshold, round_p)
+                               threshold, p_type)
                 Os.append(o_)
                 Ls.append(l_)
             if not Os:
@@ -121,7 +131,7 @@ def decode(q, k_cache, v_cache, seqlens, ranges, *, scale, causal=False, thresho
             with np.errstate(divide="ignore", invalid="ignore"):
                 O = np.where(W[:, None] > 0, f32(acc * f32(np.float32(1) / W)[:, None]), np.float32(0))
                 lrow = np.where(W > 0, M + LN2 * np.log2(W), -np.inf)
-            O = to_bf16(O) if out16 else O
+            O = ROUND[out_type](O)
             out[b, :, h * G:(h + 1) * G] = O.reshape(nq, G, d)
             lse[b, :, h * G:(h + 1) * G] = lrow.reshape(nq, G)
     return out, lse

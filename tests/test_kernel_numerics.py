@@ -24,14 +24,15 @@ from tests.tolerances import REG_ABS, REG_LONG, REG_LSE
 SHORT = workloads.shrink(workloads.CONFIGS["llama8b"], batch=2, seqlen=700)  # scale 0.3: peaked rows
 
 
-def _run(cfg, splits, *, scale=0.0, out16=True, threshold=8.0, round_p=True):
-    return _compare(workloads.make_inputs(cfg), splits, scale=scale, causal=cfg.causal, out16=out16,
-                    threshold=threshold, round_p=round_p)
+def _run(cfg, splits, *, scale=0.0, threshold=8.0, p_type="bf16", out_type="bf16", dtype=torch.bfloat16):
+    return _compare(workloads.make_inputs(cfg, dtype=dtype), splits, scale=scale, causal=cfg.causal,
+                    threshold=threshold, p_type=p_type, out_type=out_type)
 
 
-def _compare(inp, splits, *, scale=0.0, causal=False, out16=True, threshold=8.0, round_p=True):
-    """Max error of the model against the oracle: |dO| (beyond one bf16 ulp
-    for 16-bit outputs) and |dlse|, with `splits` pieces per sequence."""
+def _compare(inp, splits, *, scale=0.0, causal=False, threshold=8.0, p_type="bf16", out_type="bf16"):
+    """Max error of the model against the oracle: |dO| (beyond one ulp of
+    the output type for 16-bit outputs) and |dlse|, with `splits` pieces per
+    sequence."""
     sc = scale if scale else 1.0 / float(inp.q.shape[-1]) ** 0.5
     ref_o, ref_l = oracle.decode(inp.q, inp.k_cache, inp.v_cache, inp.seqlens, scale=sc, causal=causal)
     begin, end = oracle.split_ranges(inp.seqlens.tolist(), splits)
@@ -41,13 +42,14 @@ def _compare(inp, splits, *, scale=0.0, causal=False, out16=True, threshold=8.0,
 
     o, l = km.decode(inp.q.float().numpy(), inp.k_cache.float().numpy(), inp.v_cache.float().numpy(),
                      inp.seqlens.numpy(), ranges, scale=sc, causal=causal, threshold=threshold,
-                     out16=out16, round_p=round_p)
+                     p_type=p_type, out_type=out_type)
     fin = ~np.isneginf(ref_l)
     assert np.array_equal(np.isneginf(l), ~fin)
     diff = np.abs(o - ref_o)
-    if out16:  # beyond one bf16 ulp of the reference, as the GPU tests measure it
-        ax = np.maximum(np.abs(ref_o), 2.0 ** -126)
-        diff = diff - np.exp2(np.floor(np.log2(ax)) - 7)
+    if out_type is not None:  # beyond one ulp of the reference, as the GPU tests measure it
+        mant, tiny = (7, 2.0 ** -126) if out_type == "bf16" else (10, 2.0 ** -14)
+        ax = np.maximum(np.abs(ref_o), tiny)
+        diff = diff - np.exp2(np.floor(np.log2(ax)) - mant)
     return float(diff.max()), float(np.abs(l[fin] - ref_l[fin]).max())
 
 
@@ -65,8 +67,8 @@ def test_model_without_its_roundings_matches_the_oracle(name, splits):
     cfg = {"short": SHORT,
            "spec-edge": workloads.shrink(workloads.CONFIGS["spec"], batch=5, seqlen=1000)}.get(
         name, workloads.CONFIGS.get(name))
-    err_o, err_l = _run(cfg, splits, scale=0.3 if name == "short" else 0.0, out16=False, threshold=0.0,
-                        round_p=False)
+    err_o, err_l = _run(cfg, splits, scale=0.3 if name == "short" else 0.0, threshold=0.0, p_type=None,
+                        out_type=None)
     assert err_o < 1e-5 and err_l < 1e-5  # fp32 round-off; the modelled roundings cost 1e-4 to 5e-3
 
 
@@ -74,9 +76,9 @@ def test_stale_max_sets_the_short_row_bound():
     """Peaked rows (scale 0.3, 700 keys, four pieces per pair, as the
     automatic plan takes them): the error with the threshold-8 max is several
     times the error with a current max, and both stay under REG_ABS."""
-    stale, lse_err = _run(SHORT, 4, scale=0.3, out16=False)
-    current, _ = _run(SHORT, 4, scale=0.3, out16=False, threshold=0.0)
-    stale16, _ = _run(SHORT, 4, scale=0.3, out16=True)
+    stale, lse_err = _run(SHORT, 4, scale=0.3, out_type=None)
+    current, _ = _run(SHORT, 4, scale=0.3, out_type=None, threshold=0.0)
+    stale16, _ = _run(SHORT, 4, scale=0.3)
     assert 2e-3 < stale < REG_ABS
     assert current < stale / 2
     assert stale16 < REG_ABS and lse_err < REG_LSE
@@ -95,5 +97,16 @@ def test_head_dim_256_rows(which, splits):
     largest error is in its 129-key sequence, a short row whose two pieces
     each take their max exactly: plain bf16 rounding of p, 7.8e-4, with
     only a 1.3x margin to the bound, so the model pins that margin here."""
-    err_o, err_l = _compare(workloads.head_dim_256_inputs(which), splits, out16=False)
+    err_o, err_l = _compare(workloads.head_dim_256_inputs(which), splits, out_type=None)
     assert err_o < (REG_LONG / 4 if which == 0 else REG_LONG) and err_l < REG_LSE / 4
+
+
+@pytest.mark.parametrize("name", ["llama8b", "spec"])
+def test_fp16_inputs_round_p_three_bits_finer(name):
+    """fp16 inputs: P enters the value product in fp16 (10 mantissa bits
+    against bf16's 7), so the same shapes drawn in fp16 err several times
+    less, far under the long-row bound."""
+    cfg = workloads.CONFIGS[name]
+    e16, l16 = _run(cfg, 2, p_type="fp16", out_type=None, dtype=torch.float16)
+    e_bf, _ = _run(cfg, 2, p_type="bf16", out_type=None)
+    assert e16 < e_bf / 4 and e16 < REG_LONG / 10 and l16 < REG_LSE / 4
