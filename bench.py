@@ -119,9 +119,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source."""
+def ncu_fields(workload: str):
+    """The machine-read fields ("- key: `value`" lines) of the committed ncu
+    summary of the decode kernel on `workload`, and its path, if the summary
+    was taken on the current kernel source; else (None, why)."""
     path = os.path.join(PROFILES, f"decode_kernel_{workload}.md")
     try:
         with open(path) as f:
@@ -132,13 +133,36 @@ def ncu_traffic(workload: str):
     for line in text.splitlines():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
+            v = v.strip()
+            if v.startswith("`") and "`" in v[1:]:  # the quoted value, without any remark after it
+                v = v[1:v.index("`", 1)]
+            fields[k.strip()] = v
     if fields.get("kernel_source_sha256") != kernel_source_digest():
         return None, "kernel changed since the ncu capture"
+    return fields, os.path.relpath(path, ROOT)
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    fields, src = ncu_fields(workload)
+    if fields is None:
+        return None, src
     try:
-        return float(fields["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
+        return float(fields["dram_bytes_per_launch"]), src
     except (KeyError, ValueError):
         return None, "summary has no dram_bytes_per_launch"
+
+
+def ncu_tensor_pct(workload: str):
+    """The decode kernel's tensor-pipe utilisation (sm__pipe_tensor_cycles_active,
+    % of peak sustained over the launch) from the committed ncu summary, if
+    it was taken on the current kernel source; else None."""
+    fields, _ = ncu_fields(workload)
+    try:
+        return float(fields["tensor_pipe_active_pct"]) if fields is not None else None
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
@@ -450,12 +474,14 @@ def bench_ours(args, cfg, world, rank, local):
     achieved = kv_bytes / (ms_decode * 1e-3) / 1e9
     if args.len_div == 1:
         traffic, traffic_src = ncu_traffic(cfg.name)
+        tensor_pct = ncu_tensor_pct(cfg.name)
     else:
         traffic, traffic_src = None, "lengths divided for a profiling capture"
+        tensor_pct = None
     roofline = {"bound": "hbm", "kernel": "gqa_decode_kernel", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                "traffic": traffic, "traffic_source": traffic_src, "us_per_launch": round(ms_decode * 1e3, 3),
-                "algorithmic_bytes_per_launch": kv_bytes}
+                "traffic": traffic, "traffic_source": traffic_src, "tensor_pipe_active_pct": tensor_pct,
+                "us_per_launch": round(ms_decode * 1e3, 3), "algorithmic_bytes_per_launch": kv_bytes}
     value = world * kv_bytes / (ms_step_max * 1e-3) / 1e9
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1,7 +1,8 @@
 """The ncu summaries under profiles/ are tied to the decode kernel's code by a
 digest that ignores comments and layout: the committed summaries match the
 committed sources, a comment edit keeps the digest, a code edit changes it,
-and bench.py reads a summary's DRAM bytes only while they match."""
+and bench.py reads a summary's DRAM bytes and tensor-pipe utilisation only
+while they match."""
 import glob
 import os
 
@@ -23,6 +24,8 @@ def test_committed_summaries_match_the_kernel_sources():
         if traffic is None and "changed" in source:
             pytest.skip(f"kernel code {digest} differs from the ncu summaries: re-capture them")
         assert traffic is not None and traffic > 0, (path, source, digest)
+        tensor = bench.ncu_tensor_pct(workload)  # reported beside the DRAM figure
+        assert tensor is not None and 0 < tensor < 100, (path, tensor)
 
 
 def test_code_only_ignores_comments_and_layout():
@@ -48,9 +51,14 @@ def test_summary_ignored_once_the_code_changes(tmp_path, monkeypatch):
     (prof / "decode_kernel_ragged.md").write_text(
         f"- kernel_source_sha256: `{bench.kernel_source_digest()}`\n- dram_bytes_per_launch: `930257664`\n")
     assert bench.ncu_traffic("ragged")[0] == 930257664.0
+    assert bench.ncu_tensor_pct("ragged") is None  # no such field: reported as null
+    with open(prof / "decode_kernel_ragged.md", "a") as f:
+        f.write("- tensor_pipe_active_pct: `3.1` (a remark after the value)\n")
+    assert bench.ncu_tensor_pct("ragged") == 3.1
     k = src / "decode_kernel.cuh"
     k.write_text(k.read_text() + "\n// a comment\n")
     assert bench.ncu_traffic("ragged")[0] is not None
     k.write_text(k.read_text() + "\nstatic_assert(true, \"\");\n")
     traffic, why = bench.ncu_traffic("ragged")
     assert traffic is None and "changed" in why
+    assert bench.ncu_tensor_pct("ragged") is None
